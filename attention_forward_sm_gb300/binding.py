@@ -1,0 +1,143 @@
+"""ctypes binding of libattn.so (include/attn.h).
+
+Argument marshalling only: tensors become device pointers, the torch stream
+becomes a ``cudaStream_t``; every step of the computation runs in the
+library's CUDA kernels.  There is no fallback: if the library is missing or
+cannot be loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libattn.so")
+
+ATTN_STATUS = {
+    0: "ATTN_OK", -1: "ATTN_ERR_NULL", -2: "ATTN_ERR_ALIGN", -3: "ATTN_ERR_SHAPE",
+    -4: "ATTN_ERR_DEVICE", -5: "ATTN_ERR_LAUNCH", -6: "ATTN_ERR_ALLOC", -7: "ATTN_ERR_TMA",
+    -8: "ATTN_ERR_CUDA",
+}
+EXPORTED = ["attn_fwd", "attn_decode_splitkv", "attn_status_string", "attn_get_device_error",
+            "attn_decode_workspace_bytes"]
+
+_lock = threading.Lock()
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(msg)
+        self.status = status
+
+
+def load(path: str = LIB_PATH):
+    """Load libattn.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with "
+                               "`python -m attention_forward_sm_gb300._build`")
+        lib = ctypes.CDLL(path)
+        vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+        lib.attn_fwd.restype = i
+        lib.attn_decode_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, vp]
+        lib.attn_decode_splitkv.restype = i
+        lib.attn_status_string.argtypes = [i]
+        lib.attn_status_string.restype = ctypes.c_char_p
+        lib.attn_get_device_error.argtypes = [vp]
+        lib.attn_get_device_error.restype = i
+        lib.attn_decode_workspace_bytes.argtypes = [i, i, i, i]
+        lib.attn_decode_workspace_bytes.restype = ctypes.c_longlong
+        _lib = lib
+        return lib
+
+
+def _ptr(x) -> int:
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(rc: int):
+    if rc != 0:
+        msg = load().attn_status_string(rc).decode()
+        raise AttnError(rc, msg)
+
+
+# ----------------------------------------------------------------------------- C-ABI names
+
+
+def attn_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, causal, scale, stream=None) -> None:
+    """``attn_fwd`` of include/attn.h: tensors (or raw device pointers), sizes,
+    causal flag, scale, and a torch stream / raw handle (None = current)."""
+    _check(load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(Hq),
+                           int(Hkv), int(Nq), int(Nk), int(D), int(bool(causal)), float(scale),
+                           _stream(stream)))
+
+
+def attn_decode_splitkv(q, kcache, vcache, o, lse, B, Hq, Hkv, Nk, D, nsplit, stream=None) -> None:
+    """``attn_decode_splitkv`` of include/attn.h."""
+    _check(load().attn_decode_splitkv(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(o), _ptr(lse),
+                                      int(B), int(Hq), int(Hkv), int(Nk), int(D), int(nsplit),
+                                      _stream(stream)))
+
+
+def attn_status_string(status: int) -> str:
+    return load().attn_status_string(int(status)).decode()
+
+
+def attn_get_device_error(stream=None) -> int:
+    """Synchronise the stream, return and clear the device error word."""
+    rc = load().attn_get_device_error(_stream(stream))
+    if rc < 0:
+        _check(rc)
+    return rc
+
+
+def attn_decode_workspace_bytes(B, Hq, D, nsplit) -> int:
+    return int(load().attn_decode_workspace_bytes(int(B), int(Hq), int(D), int(nsplit)))
+
+
+# ----------------------------------------------------------------------------- tensor helpers
+
+
+def forward(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
+    """O, LSE = attention(q [B,Hq,Nq,D], k/v [B,Hkv,Nk,D]) with outputs
+    allocated by torch on q's device."""
+    import torch
+    B, Hq, Nq, D = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+    attn_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, causal, scale, stream)
+    return o, lse
+
+
+def decode(q, kcache, vcache, nsplit: int, stream=None):
+    """O, LSE = split-KV decode(q [B,Hq,D], caches [B,Hkv,Nk,D])."""
+    import torch
+    B, Hq, D = q.shape
+    Hkv, Nk = kcache.shape[1], kcache.shape[2]
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    attn_decode_splitkv(q, kcache, vcache, o, lse, B, Hq, Hkv, Nk, D, nsplit, stream)
+    return o, lse

@@ -1,0 +1,521 @@
+// Attention forward (prefill) for sm_103a: tiled, IO-aware, online softmax,
+// per-row log-sum-exp, causal mask and grouped KV heads.
+//
+// Method.  FlashAttention computes softmax(scale * Q K^T) V tile by tile
+// without writing the N x N score matrix to HBM ("FlashAttention-3 vs Triton
+// Kernels", introduction).  Each query row keeps a running max m and running
+// sum l; when m grows the accumulated output is rescaled ("correction"
+// partition in "Warp Specialization in Triton: Design and Roadmap", "How the
+// compiler does it").  The kernel is warp-specialised: load, MMA, softmax,
+// correction and epilogue run in different warps and talk through mbarrier
+// producer/consumer pipes, so loads, tensor-core work and exponentials
+// overlap (same note, and the pipeline diagram and "Hardware Mechanics" of the
+// FlashAttention-3 page, which describe the Hopper version of the idea).
+//
+// GB300 design (not the Hopper layout of the pages):
+//   * one CTA = 2 query tiles of 128 rows of one (batch, head); the two tiles
+//     are independent MMA chains (the autoWS note's "data partitioning"), so
+//     the tensor core works on one tile while the softmax of the other runs;
+//   * tcgen05.mma (kind::f16, M=128) issued by a single thread; S = Q K^T and
+//     O accumulate in tensor memory (TMEM), not registers: S0, S1, O0, O1
+//     occupy 128 + 128 + D + D of the 512 TMEM columns;
+//   * P (bf16) is written back over S in TMEM and fed to the P*V MMA as the
+//     A operand straight from TMEM;
+//   * a TMA load warp streams K and V tiles (128 keys x D, 128-byte swizzle)
+//     through a STAGES-deep shared-memory ring;
+//   * two softmax warpgroups (thread = query row) compute row max, exp2,
+//     row sum in fp32 and publish the rescale factor; a correction warpgroup
+//     rescales O in TMEM only when some row's max rose by more than 2^8
+//     (otherwise the stale max stays: exact, because the final division uses
+//     the same max), then does the epilogue (O / l -> bf16 -> swizzled smem ->
+//     TMA store, and LSE);
+//   * setmaxnreg moves registers from the load/MMA warps to the softmax warps.
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int kBM = 128;          // query rows per tile
+constexpr int kBN = 128;          // keys per K/V tile
+constexpr int kThreads = 512;     // 16 warps
+constexpr int kWarpLoad = 12;
+constexpr int kWarpMma = 13;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max rises > 2^8
+
+template <int D>
+struct Cfg {
+  static constexpr int kTileBytes = kBM * D * 2;      // one 128 x D bf16 tile
+  static constexpr int kChunks = D / 64;              // 64-column swizzle chunks per tile
+  static constexpr int kStages = (D == 128) ? 4 : 8;  // K/V ring depth
+  static constexpr int kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
+  static constexpr int kTmemCols = 512;
+  // shared memory map (offsets from a 1024-byte aligned base)
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffKV = 2 * kTileBytes;
+  static constexpr int kOffMisc = kOffKV + kStages * kTileBytes;
+  static constexpr int kMiscBytes = 4096;
+  static constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;  // + alignment slack
+};
+
+struct Misc {
+  uint64_t q_full;
+  uint64_t s_full[2], p_full[2], o_full[2], o_corr[2], stats[2], fin_full[2];
+  uint64_t mma_done;
+  uint64_t kv_full[8], kv_empty[8];
+  uint32_t tmem_base;
+  int abort_flag;
+  float alpha[2][kBM];
+  float m_fin[2][kBM];
+  float l_fin[2][kBM];
+};
+static_assert(sizeof(Misc) <= 4096, "misc region");
+
+__device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xFFFFFFFFu, v); }
+
+// Wait used only while tearing down after an abort: ignores the abort flag and
+// gives up after a bounded number of polls (each poll suspends briefly), so
+// copies and MMAs already in flight retire before the CTA exits.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  for (int spin = 0; spin < (1 << 20); ++spin)
+    if (mbar_try_wait(bar, parity)) return;
+}
+
+// 64 consecutive TMEM columns of this thread's lane from registers, one wait.
+#define ATTN_W8(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), "r"(r[i + 4]), \
+    "r"(r[i + 5]), "r"(r[i + 6]), "r"(r[i + 7])
+__device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&r)[64]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%64], {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, "
+      "%10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, "
+      "%27, %28, %29, %30, %31};\n\t"
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%65], {%32, %33, %34, %35, %36, %37, %38, %39, "
+      "%40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, "
+      "%57, %58, %59, %60, %61, %62, %63};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::ATTN_W8(0),
+      ATTN_W8(8), ATTN_W8(16), ATTN_W8(24), ATTN_W8(32), ATTN_W8(40), ATTN_W8(48), ATTN_W8(56),
+      "r"(taddr), "r"(taddr + 32)
+      : "memory");
+}
+#undef ATTN_W8
+
+// 128 consecutive TMEM columns of this thread's lane, one wait.
+#define ATTN_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), \
+    "=r"(r[i + 4]), "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31}, [%128];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32, %33, %34, %35, %36, %37, %38, %39, %40, "
+      "%41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, "
+      "%58, %59, %60, %61, %62, %63}, [%129];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%64, %65, %66, %67, %68, %69, %70, %71, %72, "
+      "%73, %74, %75, %76, %77, %78, %79, %80, %81, %82, %83, %84, %85, %86, %87, %88, %89, "
+      "%90, %91, %92, %93, %94, %95}, [%130];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%96, %97, %98, %99, %100, %101, %102, %103, "
+      "%104, %105, %106, %107, %108, %109, %110, %111, %112, %113, %114, %115, %116, %117, "
+      "%118, %119, %120, %121, %122, %123, %124, %125, %126, %127}, [%131];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : ATTN_R8(0), ATTN_R8(8), ATTN_R8(16), ATTN_R8(24), ATTN_R8(32), ATTN_R8(40), ATTN_R8(48),
+        ATTN_R8(56), ATTN_R8(64), ATTN_R8(72), ATTN_R8(80), ATTN_R8(88), ATTN_R8(96),
+        ATTN_R8(104), ATTN_R8(112), ATTN_R8(120)
+      : "r"(taddr), "r"(taddr + 32), "r"(taddr + 64), "r"(taddr + 96)
+      : "memory");
+}
+#undef ATTN_R8
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ FwdParams p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  Misc& ms = *reinterpret_cast<Misc*>(smem + C::kOffMisc);
+  volatile int* abort_flag = &ms.abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- work unit: (batch*head, pair of 128-row query tiles)
+  const int nqb = (p.Nq + 2 * kBM - 1) / (2 * kBM);
+  int qblk = static_cast<int>(blockIdx.x % nqb);
+  const int bh = static_cast<int>(blockIdx.x / nqb);
+  if (p.causal) qblk = nqb - 1 - qblk;  // longest rows first
+  const int q_base = qblk * 2 * kBM;
+  const int G = p.Hq / p.Hkv;
+  const int bhkv = (bh / p.Hq) * p.Hkv + (bh % p.Hq) / G;
+  int n_kv = (p.Nk + kBN - 1) / kBN;
+  if (p.causal) n_kv = min(n_kv, (q_base + 2 * kBM + kBN - 1) / kBN);
+
+  // ---- setup: barriers (loader warp), TMEM (MMA warp)
+  if (warp == kWarpLoad && lane == 0) {
+    mbar_init(&ms.q_full, 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&ms.s_full[t], 1);
+      mbar_init(&ms.p_full[t], kBM);
+      mbar_init(&ms.o_full[t], 1);
+      mbar_init(&ms.o_corr[t], kBM);
+      mbar_init(&ms.stats[t], kBM);
+      mbar_init(&ms.fin_full[t], kBM);
+    }
+    mbar_init(&ms.mma_done, 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&ms.kv_full[s], 1);
+      mbar_init(&ms.kv_empty[s], 1);
+    }
+    ms.abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&p.tmap_q);
+    tma_prefetch_desc(&p.tmap_k);
+    tma_prefetch_desc(&p.tmap_v);
+    tma_prefetch_desc(&p.tmap_o);
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(&ms.tmem_base, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ms.tmem_base;
+  const uint64_t lim = p.wait_limit_ns;
+
+  if (warp < 8) {
+    // =====================================================================
+    // softmax warpgroup t: thread = query row r of tile t
+    // =====================================================================
+    reg_alloc<184>();
+    const int t = warp >> 2;
+    const int r = (warp & 3) * 32 + lane;
+    const int row = q_base + t * kBM + r;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const uint32_t s_addr = lane_addr + (t ? C::kColS1 : C::kColS0);
+    const int tile_row0 = q_base + t * kBM;
+    const int vis = p.causal ? min(row + 1, p.Nk) : p.Nk;  // keys [0, vis) visible
+    float m = -CUDART_INF_F, l = 0.f;
+    for (int j = 0; j < n_kv; ++j) {
+      if (!warp_all(mbar_wait(&ms.s_full[t], j & 1, abort_flag, p.err, kErrWaitSoftmax, lim)))
+        break;
+      tc_fence_after();
+      uint32_t sr[128];
+      tmem_ld128(s_addr, sr);
+      float s[kBN];
+#pragma unroll
+      for (int c = 0; c < kBN; ++c) s[c] = __uint_as_float(sr[c]);
+      const int kb = j * kBN;
+      const bool need_mask = (kb + kBN > p.Nk) || (p.causal && kb + kBN - 1 > tile_row0);
+      float mx;
+      if (need_mask) {
+        const int lim_c = vis - kb;  // columns [0, lim_c) valid
+#pragma unroll
+        for (int c = 0; c < kBN; ++c)
+          if (c >= lim_c) s[c] = -CUDART_INF_F;
+      }
+      {
+        float a0 = s[0], a1 = s[1], a2 = s[2], a3 = s[3];
+#pragma unroll
+        for (int c = 4; c < kBN; c += 4) {
+          a0 = fmaxf(a0, s[c]);
+          a1 = fmaxf(a1, s[c + 1]);
+          a2 = fmaxf(a2, s[c + 2]);
+          a3 = fmaxf(a3, s[c + 3]);
+        }
+        mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
+      }
+      // running max in log2 units (scale >= 0, so max commutes with scaling)
+      const float m_tile = (mx == -CUDART_INF_F) ? -CUDART_INF_F : mx * p.scale_log2;
+      float alpha = 1.f;
+      if (m_tile > m + kRescaleThreshold || m == -CUDART_INF_F) {
+        alpha = ex2_approx(m - m_tile);  // 0 on the first tile
+        m = m_tile;
+      }
+      if (j > 0) {
+        ms.alpha[t][r] = alpha;
+        mbar_arrive(&ms.stats[t]);
+      }
+      // p = 2^(s*scale*log2e - m), masked entries exactly 0
+      const float neg_m = -m;
+      float rs0 = 0.f, rs1 = 0.f;
+      uint32_t pk[64];
+      if (need_mask) {
+#pragma unroll
+        for (int c = 0; c < kBN; c += 2) {
+          const float p0 =
+              (s[c] == -CUDART_INF_F) ? 0.f : ex2_approx(fmaf(s[c], p.scale_log2, neg_m));
+          const float p1 = (s[c + 1] == -CUDART_INF_F)
+                               ? 0.f
+                               : ex2_approx(fmaf(s[c + 1], p.scale_log2, neg_m));
+          rs0 += p0;
+          rs1 += p1;
+          pk[c / 2] = pack_bf16x2(p0, p1);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < kBN; c += 2) {
+          const float p0 = ex2_approx(fmaf(s[c], p.scale_log2, neg_m));
+          const float p1 = ex2_approx(fmaf(s[c + 1], p.scale_log2, neg_m));
+          rs0 += p0;
+          rs1 += p1;
+          pk[c / 2] = pack_bf16x2(p0, p1);
+        }
+      }
+      l = fmaf(l, alpha, rs0 + rs1);
+      // P (bf16 pairs) over the first 64 columns of S
+      tmem_st64(s_addr, pk);
+      tc_fence_before();
+      mbar_arrive(&ms.p_full[t]);
+    }
+    if (!*abort_flag) {
+      ms.m_fin[t][r] = m;
+      ms.l_fin[t][r] = l;
+      mbar_arrive(&ms.fin_full[t]);
+    }
+  } else if (warp < 12) {
+    // =====================================================================
+    // correction + epilogue warpgroup: thread = row r of both tiles
+    // =====================================================================
+    reg_dealloc<88>();
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    bool ok = true;
+    for (int j = 1; j < n_kv && ok; ++j) {
+      for (int t = 0; t < 2 && ok; ++t) {
+        ok = warp_all(
+            mbar_wait(&ms.stats[t], (j - 1) & 1, abort_flag, p.err, kErrWaitCorr, lim));
+        if (!ok) break;
+        const float a = ms.alpha[t][r];
+        if (__any_sync(0xFFFFFFFFu, a != 1.f)) {
+          ok = warp_all(
+              mbar_wait(&ms.o_full[t], (j - 1) & 1, abort_flag, p.err, kErrWaitCorr, lim));
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t o_addr = lane_addr + (t ? C::kColO1 : C::kColO0);
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(o_addr + c * 32, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * a);
+            tmem_st32(o_addr + c * 32, v);
+          }
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        mbar_arrive(&ms.o_corr[t]);
+      }
+    }
+    // epilogue: O / l -> bf16 -> swizzled smem (the tile's Q buffer) -> TMA store
+    for (int t = 0; t < 2; ++t) {
+      bool good = ok && warp_all(mbar_wait(&ms.fin_full[t], 0, abort_flag, p.err,
+                                           kErrWaitCorr, lim));
+      good = good && warp_all(mbar_wait(&ms.o_full[t], (n_kv - 1) & 1, abort_flag, p.err,
+                                        kErrWaitCorr, lim));
+      uint8_t* stage = smem + C::kOffQ + t * C::kTileBytes;
+      if (good) {
+        tc_fence_after();
+        const float mrow = ms.m_fin[t][r];
+        const float lrow = ms.l_fin[t][r];
+        const float inv = 1.f / lrow;
+        const uint32_t o_addr = lane_addr + (t ? C::kColO1 : C::kColO0);
+        const uint32_t stage_row = smem_u32(stage) + r * 128;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(o_addr + c * 32, v);
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            w[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * inv, __uint_as_float(v[2 * i + 1]) * inv);
+          const uint32_t chunk_base = stage_row + (c >> 1) * (kBM * 128);
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const int gran = (c & 1) * 4 + g;
+            const uint32_t addr = chunk_base + ((gran ^ (r & 7)) << 4);
+            st_shared_v4(addr, w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
+          }
+        }
+        const int row = q_base + t * kBM + r;
+        if (row < p.Nq)
+          p.lse[static_cast<size_t>(bh) * p.Nq + row] =
+              (mrow + __log2f(lrow)) * 0.69314718055994530942f;
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1, 128);
+      if (warp == 8 && lane == 0 && !*abort_flag && q_base + t * kBM < p.Nq) {
+#pragma unroll
+        for (int ch = 0; ch < C::kChunks; ++ch)
+          tma_store_3d(&p.tmap_o, stage + ch * (kBM * 128), ch * 64, q_base + t * kBM, bh);
+        tma_store_commit();
+      }
+    }
+    if (warp == 8 && lane == 0) tma_store_wait_all0();
+  } else if (warp == kWarpLoad) {
+    // =====================================================================
+    // TMA loader: Q tiles once, then K_j, V_j through the ring
+    // =====================================================================
+    reg_dealloc<56>();
+    if (lane == 0) {
+      const uint64_t pol_q = l2_policy_evict_first();
+      const uint64_t pol_kv = l2_policy_evict_last();
+      mbar_arrive_expect_tx(&ms.q_full, 2 * C::kTileBytes);
+      for (int t = 0; t < 2; ++t)
+        for (int ch = 0; ch < C::kChunks; ++ch)
+          tma_load_3d(smem + C::kOffQ + t * C::kTileBytes + ch * (kBM * 128), &p.tmap_q,
+                      &ms.q_full, ch * 64, q_base + t * kBM, bh, pol_q);
+      int issued = 0;
+      for (int it = 0; it < 2 * n_kv; ++it) {
+        const int s = it % C::kStages;
+        const uint32_t ph = static_cast<uint32_t>(it / C::kStages) & 1u;
+        if (!mbar_wait(&ms.kv_empty[s], ph ^ 1u, abort_flag, p.err, kErrWaitLoad, lim)) break;
+        mbar_arrive_expect_tx(&ms.kv_full[s], C::kTileBytes);
+        const CUtensorMap* map = (it & 1) ? &p.tmap_v : &p.tmap_k;
+        uint8_t* dst = smem + C::kOffKV + s * C::kTileBytes;
+        for (int ch = 0; ch < C::kChunks; ++ch)
+          tma_load_3d(dst + ch * (kBM * 128), map, &ms.kv_full[s], ch * 64, (it >> 1) * kBN, bhkv,
+                      pol_kv);
+        issued = it + 1;
+      }
+      if (*abort_flag) {
+        // drain: wait (bounded) for the copies still in flight before exiting
+        drain_wait(&ms.q_full, 0);
+        for (int it = max(0, issued - C::kStages); it < issued; ++it)
+          drain_wait(&ms.kv_full[it % C::kStages],
+                     static_cast<uint32_t>(it / C::kStages) & 1u);
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // =====================================================================
+    // MMA issuer (one thread): S_t = Q_t K_j^T, O_t += P_t V_j
+    // =====================================================================
+    reg_dealloc<56>();
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, kBN, false);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
+      const uint32_t q_addr = smem_u32(smem + C::kOffQ);
+      const uint32_t kv_addr = smem_u32(smem + C::kOffKV);
+      bool ok = mbar_wait(&ms.q_full, 0, abort_flag, p.err, kErrWaitMma, lim);
+      // P_t V_{jv} into O_t
+      auto issue_pv = [&](int t, int jv) -> bool {
+        if (!mbar_wait(&ms.p_full[t], jv & 1, abort_flag, p.err, kErrWaitMma, lim)) return false;
+        if (jv > 0 &&
+            !mbar_wait(&ms.o_corr[t], (jv - 1) & 1, abort_flag, p.err, kErrWaitMma, lim))
+          return false;
+        tc_fence_after();
+        const int itv = 2 * jv + 1;
+        const uint32_t v_base = kv_addr + (itv % C::kStages) * C::kTileBytes;
+        const uint32_t p_tmem = tmem + (t ? C::kColS1 : C::kColS0);
+        const uint32_t o_tmem = tmem + (t ? C::kColO1 : C::kColO0);
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          const uint64_t b = sdesc_sw128(v_base + kk * 16 * 128, kBM * 128, 1024);
+          mma_ts(o_tmem, p_tmem + kk * 8, b, idesc_pv, (jv > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&ms.o_full[t]);
+        return true;
+      };
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const int itk = 2 * j;
+        const int sk = itk % C::kStages;
+        ok = mbar_wait(&ms.kv_full[sk], static_cast<uint32_t>(itk / C::kStages) & 1u, abort_flag,
+                       p.err, kErrWaitMma, lim);
+        if (!ok) break;
+        int sv = 0;
+        if (j > 0) {
+          const int itv = 2 * (j - 1) + 1;
+          sv = itv % C::kStages;
+          ok = mbar_wait(&ms.kv_full[sv], static_cast<uint32_t>(itv / C::kStages) & 1u,
+                         abort_flag, p.err, kErrWaitMma, lim);
+          if (!ok) break;
+        }
+        tc_fence_after();
+        const uint32_t k_base = kv_addr + sk * C::kTileBytes;
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (j > 0) ok = issue_pv(t, j - 1);
+          if (!ok) break;
+          const uint32_t q_base_addr = q_addr + t * C::kTileBytes;
+          const uint32_t s_tmem = tmem + (t ? C::kColS1 : C::kColS0);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
+            const uint64_t a = sdesc_sw128(q_base_addr + off, 16, 1024);
+            const uint64_t b = sdesc_sw128(k_base + off, 16, 1024);
+            mma_ss(s_tmem, a, b, idesc_s, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&ms.s_full[t]);
+        }
+        if (!ok) break;
+        mma_commit(&ms.kv_empty[sk]);
+        if (j > 0) mma_commit(&ms.kv_empty[sv]);
+      }
+      if (ok) {
+        const int itv = 2 * (n_kv - 1) + 1;
+        const int sv = itv % C::kStages;
+        ok = mbar_wait(&ms.kv_full[sv], static_cast<uint32_t>(itv / C::kStages) & 1u, abort_flag,
+                       p.err, kErrWaitMma, lim);
+        if (ok) {
+          tc_fence_after();
+          for (int t = 0; t < 2 && ok; ++t) ok = issue_pv(t, n_kv - 1);
+          if (ok) mma_commit(&ms.kv_empty[sv]);
+        }
+      }
+      // all issued MMAs retire before the CTA releases TMEM
+      mma_commit(&ms.mma_done);
+      drain_wait(&ms.mma_done, 0);
+    }
+  } else {
+    reg_dealloc<56>();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_d(const FwdParams& p, cudaStream_t stream) {
+  using C = Cfg<D>;
+  // the shared-memory opt-in is a per-device property of the function
+  static bool attr_done[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_done[dev]) {
+    e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  const long long nqb = (p.Nq + 2 * kBM - 1) / (2 * kBM);
+  const long long grid = nqb * p.B * p.Hq;
+  attn_fwd_kernel<D><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t fwd_smem_bytes(int D) {
+  return D == 128 ? Cfg<128>::kSmemBytes : Cfg<64>::kSmemBytes;
+}
+
+cudaError_t launch_fwd(const FwdParams& p, cudaStream_t stream) {
+  if (p.D == 128) return launch_d<128>(p, stream);
+  if (p.D == 64) return launch_d<64>(p, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace attn

@@ -1,0 +1,51 @@
+// Host-side interface between the C ABI (api.cu) and the kernel translation
+// units (fwd_sm103a.cu, decode_sm103a.cu).  Not part of the public header.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace attn {
+
+// Bits of the device error word (also listed in include/attn.h).
+enum : unsigned int {
+  kErrWaitLoad = 1u << 0,     // loader gave up waiting for a free K/V slot
+  kErrWaitMma = 1u << 1,      // MMA issuer gave up waiting for data / P / correction
+  kErrWaitSoftmax = 1u << 2,  // softmax gave up waiting for S
+  kErrWaitCorr = 1u << 3,     // correction / epilogue gave up waiting
+};
+
+// Forward (prefill) launch parameters.  Tensor maps are 3-D views
+// [B*H, N, D] of the bf16 tensors, box {64, 128, 1}, 128-byte swizzle.
+struct FwdParams {
+  CUtensorMap tmap_q, tmap_k, tmap_v, tmap_o;
+  float* lse;          // [B, Hq, Nq] fp32
+  int B, Hq, Hkv, Nq, Nk, D;
+  int causal;
+  float scale_log2;    // scale * log2(e)
+  unsigned int* err;   // device error word
+  uint64_t wait_limit_ns;
+};
+
+// Split-KV decode launch parameters.
+struct DecodeParams {
+  const void* q;       // [B, Hq, D] bf16
+  const void* k;       // [B, Hkv, Nk, D] bf16
+  const void* v;       // [B, Hkv, Nk, D] bf16
+  void* o;             // [B, Hq, D] bf16
+  float* lse;          // [B, Hq] fp32
+  float* ws_o;         // [B, Hq, nsplit, D] fp32 partial outputs (normalised per chunk)
+  float* ws_lse;       // [B, Hq, nsplit] fp32 partial lse (natural log)
+  int B, Hq, Hkv, Nk, D, nsplit;
+  float scale_log2;
+};
+
+cudaError_t launch_fwd(const FwdParams& p, cudaStream_t stream);
+size_t fwd_smem_bytes(int D);
+
+cudaError_t launch_decode_split(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream);
+bool decode_supported(int G, int D);
+
+}  // namespace attn

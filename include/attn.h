@@ -1,0 +1,134 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) attention library (libattn.so).
+ *
+ * Two operations, both asynchronous on the caller's CUDA stream:
+ *
+ *   attn_fwd             tiled, IO-aware attention forward (prefill):
+ *                        O = softmax(scale * Q K^T [+ causal mask]) V and the
+ *                        per-row log-sum-exp LSE, with grouped KV heads.
+ *   attn_decode_splitkv  single-query decode over a contiguous K/V cache, the
+ *                        keys cut into nsplit chunks whose partial states are
+ *                        recombined through their LSE (split-KV / FlashDecode).
+ *
+ * Sources for the operations:
+ *   - "FlashAttention-3 vs Triton Kernels" (dailyaiworld), introduction:
+ *     FlashAttention's IO-aware tiling computes the softmax attention output
+ *     without writing the N x N score matrix to HBM; the benchmark listing in
+ *     "Benchmarking Triton vs FlashAttention-3" fixes the (batch, heads, seq,
+ *     head_dim) tensor layout and the 4*B*H*S^2*D FLOP convention.
+ *   - "Warp Specialization in Triton: Design and Roadmap" (PyTorch blog),
+ *     "How the compiler does it": the load / MMA / softmax / correction /
+ *     epilogue roles of the warp-specialised forward kernel.
+ *   - smzdm digest, section 5 ("Attention cannot be split like GEMM"): each
+ *     key shard carries an lse_i state with its output and the combine
+ *     renormalises through it; summing raw partial outputs is wrong.
+ *
+ * Numerics (identical for both calls): bf16 inputs; scores, running max,
+ * running sum and the output accumulator in fp32; the softmax probabilities
+ * are rounded to bf16 before the P*V product; O is rounded to bf16
+ * (round-to-nearest-even); LSE is fp32 in natural-log units and includes
+ * the scale:  LSE = ln sum_j exp(scale * q . k_j).
+ *
+ * Ownership: the caller allocates and owns every buffer; the library keeps
+ * no pointer after a call returns.  All pointers must be device pointers of
+ * the current CUDA device, and the stream must belong to that device.
+ *
+ * Errors: every call validates its arguments before touching the GPU and
+ * returns one of the ATTN_* codes below (0 on success).  A failed check
+ * launches nothing and writes nothing.  Faults inside a kernel surface, as
+ * for any CUDA call, at the caller's next synchronisation.  Kernels never
+ * wait forever: a pipeline wait that exceeds its time limit makes the kernel
+ * set a bit in the device error word and exit; read it with
+ * attn_get_device_error().
+ */
+#ifndef ATTN_SM103A_H_
+#define ATTN_SM103A_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The runtime's stream handle; declared here so the header does not need the
+ * CUDA headers (identical to cuda_runtime_api.h's typedef). */
+typedef struct CUstream_st *cudaStream_t;
+
+enum attn_status {
+  ATTN_OK = 0,
+  ATTN_ERR_NULL = -1,    /* a required pointer is NULL */
+  ATTN_ERR_ALIGN = -2,   /* a pointer is not 16-byte aligned (TMA needs 16 B; 128 B recommended) */
+  ATTN_ERR_SHAPE = -3,   /* a size is out of range (see each call) */
+  ATTN_ERR_DEVICE = -4,  /* current device is not compute capability 10.3 (sm_103) */
+  ATTN_ERR_LAUNCH = -5,  /* the kernel launch failed (cudaGetLastError after launch) */
+  ATTN_ERR_ALLOC = -6,   /* stream-ordered allocation of the decode scratch failed */
+  ATTN_ERR_TMA = -7,     /* cuTensorMapEncodeTiled rejected a tensor view */
+  ATTN_ERR_CUDA = -8     /* another CUDA runtime call failed */
+};
+
+/* Bits of the device error word (attn_get_device_error). */
+#define ATTN_DEVERR_WAIT_LOAD 0x1u    /* K/V loader gave up waiting for a free slot */
+#define ATTN_DEVERR_WAIT_MMA 0x2u     /* MMA issuer gave up waiting for operands */
+#define ATTN_DEVERR_WAIT_SOFTMAX 0x4u /* softmax gave up waiting for scores */
+#define ATTN_DEVERR_WAIT_CORR 0x8u    /* correction / epilogue gave up waiting */
+
+/*
+ * attn_fwd -- attention forward (prefill).
+ *
+ *   q    [B, Hq,  Nq, D] bf16, contiguous (row-major, D fastest)
+ *   k, v [B, Hkv, Nk, D] bf16, contiguous
+ *   o    [B, Hq,  Nq, D] bf16, written
+ *   lse  [B, Hq,  Nq]    fp32, written (natural log, scale included)
+ *
+ * For query head h the KV head is floor(h / (Hq / Hkv)) (contiguous groups).
+ * causal != 0: key j is visible to query row i iff j <= i (mask aligned at
+ * row 0, "top-left"); rows i >= Nk then see all keys.  scale multiplies
+ * q . k before the softmax (1/sqrt(D) is the usual choice); it must be
+ * finite and >= 0 (0 gives uniform weights over the visible keys).
+ *
+ * Limits: B, Hq, Hkv, Nq, Nk >= 1; Hq % Hkv == 0; D in {64, 128};
+ * B*Hq*ceil(Nq/256) < 2^31; every pointer 16-byte aligned; q/k/v/o must not
+ * overlap o/lse.  Returns ATTN_OK or an ATTN_ERR_* code.
+ */
+int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
+             int Hkv, int Nq, int Nk, int D, int causal, float scale, cudaStream_t stream);
+
+/*
+ * attn_decode_splitkv -- split-KV decode of one query row per (batch, head).
+ *
+ *   q       [B, Hq, D]       bf16, contiguous
+ *   kcache  [B, Hkv, Nk, D]  bf16, contiguous (head-major cache)
+ *   vcache  [B, Hkv, Nk, D]  bf16, contiguous
+ *   o       [B, Hq, D]       bf16, written
+ *   lse     [B, Hq]          fp32, written (natural log)
+ *
+ * All Nk keys are visible; the scale is 1/sqrt(D).  The key axis is cut
+ * into nsplit chunks of ceil(Nk/nsplit) keys (the last one shorter, possibly
+ * empty); each chunk yields a partial output normalised by its own softmax
+ * denominator plus its lse, and a second kernel recombines them:
+ *   L = ln sum_c exp(lse_c),   O = sum_c exp(lse_c - L) O_c.
+ * The partial states live in scratch memory the library takes from the
+ * stream-ordered allocator on `stream` and frees on `stream` after the
+ * combine (B*Hq*nsplit*(D+1)*4 bytes), so calls on different streams do not
+ * share scratch.
+ *
+ * Limits: B, Hq, Hkv, Nk >= 1; Hq % Hkv == 0; D in {64, 128};
+ * 1 <= nsplit <= Nk; B <= 65535; pointers 16-byte aligned.
+ */
+int attn_decode_splitkv(const void *q, const void *kcache, const void *vcache, void *o, float *lse,
+                        int B, int Hq, int Hkv, int Nk, int D, int nsplit, cudaStream_t stream);
+
+/* Human-readable name of an ATTN_* status code (static string). */
+const char *attn_status_string(int status);
+
+/* Synchronises `stream`, then returns the device error word of the current
+ * device (ATTN_DEVERR_* bits, 0 when no kernel gave up a wait) and clears
+ * it.  Returns a negative ATTN_ERR_* code if a CUDA call fails. */
+int attn_get_device_error(cudaStream_t stream);
+
+/* Bytes of decode scratch one attn_decode_splitkv call takes. */
+long long attn_decode_workspace_bytes(int B, int Hq, int D, int nsplit);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_SM103A_H_ */

@@ -1,0 +1,242 @@
+"""GPU parity: the CUDA library (called through its C ABI) against the CPU
+fp64 oracle on the same seeded bf16 inputs.
+
+Tolerance (per element of O): |dO| <= 2e-2 absolute OR <= 2e-2 relative to
+|O_ref|; over the checked elements mean |dO| <= 2e-3; max |dLSE| <= 1e-3
+(absolute, natural log).  Large workloads are checked on >= 4096 sampled
+query rows (row 0 and the last row always included, plus the first and last
+row of every 128-row tile of one head when causal).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from attention_forward_sm_gb300 import binding as attn
+from attention_forward_sm_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+TOL_ABS, TOL_REL, TOL_MEAN, TOL_LSE = 2e-2, 2e-2, 2e-3, 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    from attention_forward_sm_gb300 import _build
+    _build.build()
+    attn.load()
+    assert torch.cuda.is_available(), "gpu tests need a CUDA device"
+
+
+def check(o_gpu, lse_gpu, o_ref, lse_ref, label=""):
+    o = o_gpu.detach().float().cpu().numpy().astype(np.float64).reshape(o_ref.shape)
+    lse = lse_gpu.detach().float().cpu().numpy().astype(np.float64).reshape(lse_ref.shape)
+    assert np.isfinite(o).all() and np.isfinite(lse).all(), f"{label}: non-finite output"
+    err = np.abs(o - o_ref)
+    bad = (err > TOL_ABS) & (err > TOL_REL * np.abs(o_ref))
+    assert not bad.any(), (f"{label}: {int(bad.sum())} elements out of tolerance, "
+                           f"max |dO| = {err.max():.3e}")
+    assert err.mean() <= TOL_MEAN, f"{label}: mean |dO| = {err.mean():.3e}"
+    dl = np.abs(lse - lse_ref).max()
+    assert dl <= TOL_LSE, f"{label}: max |dLSE| = {dl:.3e}"
+    return err.max(), err.mean(), dl
+
+
+def run_prefill(w, q, k, v, stream=None):
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device=q.device)
+    attn.attn_fwd(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.D, w.causal, w.scale, stream)
+    torch.cuda.synchronize()
+    return o, lse
+
+
+def oracle_prefill(w, q, k, v, rows=None, scale=None):
+    s = float(np.float32(w.scale if scale is None else scale))
+    return oracle.attn_rows(q.cpu(), k.cpu(), v.cpu(), w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.D,
+                            w.causal, s, rows)
+
+
+# ----------------------------------------------------------------------------- prefill
+
+PREFILL_SHAPES = [
+    # B, Hq, Hkv, Nq, Nk, D, causal
+    (1, 2, 2, 256, 256, 64, False),
+    (2, 4, 4, 100, 100, 128, False),
+    (1, 2, 2, 129, 300, 128, True),
+    (1, 8, 2, 513, 513, 128, True),
+    (2, 4, 1, 300, 77, 64, False),
+    (1, 2, 2, 1, 1, 128, False),
+    (1, 2, 2, 1000, 1, 64, True),
+    (1, 2, 2, 700, 200, 128, True),
+    (1, 4, 4, 1024, 1024, 128, False),
+    (1, 2, 2, 2048, 2048, 64, True),
+    (1, 1, 1, 600, 4096, 128, False),
+    (1, 4, 2, 1280, 1280, 128, True),
+]
+
+
+@pytest.mark.parametrize("shape", PREFILL_SHAPES, ids=lambda s: "B{}Hq{}Hkv{}Nq{}Nk{}D{}{}".format(
+    *s[:6], "c" if s[6] else ""))
+def test_prefill_sweep(shape):
+    B, Hq, Hkv, Nq, Nk, D, causal = shape
+    w = W.custom(B, Hq, Hkv, Nq, Nk, D, causal, seed_index=hash(shape) % 1000)
+    q, k, v = (t.cuda() for t in W.make_inputs(w, "cpu"))
+    o, lse = run_prefill(w, q, k, v)
+    o_ref, lse_ref = oracle_prefill(w, q, k, v)
+    check(o, lse, o_ref.reshape(B, Hq, Nq, D), lse_ref.reshape(B, Hq, Nq), str(shape))
+
+
+def test_tiny_workload():
+    w = W.WORKLOADS["tiny"]
+    q, k, v = (t.cuda() for t in W.make_inputs(w, "cpu"))
+    o, lse = run_prefill(w, q, k, v)
+    o_ref, lse_ref = oracle_prefill(w, q, k, v)
+    check(o, lse, o_ref.reshape(o.shape), lse_ref.reshape(lse.shape), "tiny")
+
+
+@pytest.mark.parametrize("name", ["prefill", "causal", "long_gqa"])
+def test_full_size_sampled(name):
+    """The full-size workloads, same launch as the benchmark, >= 4096 sampled rows."""
+    w = W.WORKLOADS[name]
+    q, k, v = W.make_inputs(w, "cuda")
+    o, lse = run_prefill(w, q, k, v)
+    rows = W.sample_rows(w, 4096)
+    assert rows.numel() >= 4096
+    o_ref, lse_ref = oracle_prefill(w, q, k, v, rows.numpy())
+    o_s = o.reshape(-1, w.D)[rows.cuda()]
+    l_s = lse.reshape(-1)[rows.cuda()]
+    check(o_s, l_s, o_ref, lse_ref, name)
+    if w.causal:
+        # causal row 0 of every head attends to key 0 only: O = V[0] exactly (rounded to bf16)
+        G = w.Hq // w.Hkv
+        v0 = v[:, :, 0, :].repeat_interleave(G, dim=1)
+        assert torch.equal(o[:, :, 0, :], v0)
+
+
+def test_scale_zero_is_uniform():
+    """scale = 0: every visible key has the same weight (oracle and closed form)."""
+    w = W.custom(1, 2, 2, 300, 300, 128, True, seed_index=501)
+    q, k, v = (t.cuda() for t in W.make_inputs(w, "cpu"))
+    o = torch.empty_like(q)
+    lse = torch.empty((1, 2, 300), dtype=torch.float32, device="cuda")
+    attn.attn_fwd(q, k, v, o, lse, 1, 2, 2, 300, 300, 128, True, 0.0)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle_prefill(w, q, k, v, scale=0.0)
+    check(o, lse, o_ref.reshape(o.shape), lse_ref.reshape(lse.shape), "scale0")
+    np.testing.assert_allclose(lse.cpu().numpy()[0, 0], np.log(np.arange(1, 301)), atol=1e-4)
+
+
+def test_deterministic_and_stream():
+    w = W.custom(2, 8, 2, 777, 900, 128, True, seed_index=502)
+    q, k, v = (t.cuda() for t in W.make_inputs(w, "cpu"))
+    o1, l1 = run_prefill(w, q, k, v)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o2 = torch.empty_like(q)
+        l2 = torch.empty_like(l1)
+        attn.attn_fwd(q, k, v, o2, l2, w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.D, True, w.scale, s)
+    s.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_back_to_back_odd_shapes():
+    """Many launches of odd shapes in a row; the last results still match and no
+    kernel gave up a wait."""
+    shapes = [(1, 2, 1, n, n + 37, 128 if n % 2 else 64, bool(n % 3)) for n in range(1, 400, 29)]
+    data = []
+    for sh in shapes:
+        w = W.custom(*sh, seed_index=sh[3])
+        q, k, v = (t.cuda() for t in W.make_inputs(w, "cpu"))
+        data.append((w, q, k, v, torch.empty_like(q),
+                     torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device="cuda")))
+    for _ in range(20):
+        for (w, q, k, v, o, lse) in data:
+            attn.attn_fwd(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.D, w.causal, w.scale)
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_error() == 0
+    for (w, q, k, v, o, lse) in data[::3]:
+        o_ref, lse_ref = oracle_prefill(w, q, k, v)
+        check(o, lse, o_ref.reshape(o.shape), lse_ref.reshape(lse.shape), w.label())
+
+
+# ----------------------------------------------------------------------------- decode
+
+
+def run_decode(w, q, k, v, nsplit):
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=q.device)
+    attn.attn_decode_splitkv(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.Nk, w.D, nsplit)
+    torch.cuda.synchronize()
+    return o, lse
+
+
+def oracle_decode(w, q, k, v):
+    s = float(np.float32(1.0 / math.sqrt(w.D)))
+    return oracle.decode(q.cpu(), k.cpu(), v.cpu(), w.B, w.Hq, w.Hkv, w.Nk, w.D, scale=s)
+
+
+def test_decode_workload():
+    w = W.WORKLOADS["decode"]
+    q, k, v = W.make_inputs(w, "cuda")
+    o, lse = run_decode(w, q, k, v, w.nsplit)
+    o_ref, lse_ref = oracle_decode(w, q, k, v)
+    check(o, lse, o_ref.reshape(o.shape), lse_ref.reshape(lse.shape), "decode")
+
+
+DECODE_SHAPES = [
+    # B, Hq, Hkv, Nk, D, nsplit
+    (1, 4, 1, 1000, 128, 7),
+    (2, 8, 2, 9, 64, 4),        # last chunk empty (chunk = 3 keys)
+    (1, 3, 1, 513, 128, 1),     # G = 3, no split
+    (1, 16, 2, 300, 128, 300),  # one key per chunk
+    (2, 2, 2, 4096, 64, 32),    # MHA, D = 64
+    (1, 32, 2, 2048, 128, 16),  # G = 16 (two head groups per KV head)
+    (3, 12, 4, 777, 64, 5),
+]
+
+
+@pytest.mark.parametrize("shape", DECODE_SHAPES, ids=lambda s: "B{}Hq{}Hkv{}Nk{}D{}s{}".format(*s))
+def test_decode_sweep(shape):
+    B, Hq, Hkv, Nk, D, nsplit = shape
+    w = W.custom(B, Hq, Hkv, 1, Nk, D, False, seed_index=600 + Nk % 97, decode=True,
+                 nsplit=nsplit)
+    q, k, v = (t.cuda() for t in W.make_inputs(w, "cpu"))
+    o, lse = run_decode(w, q, k, v, nsplit)
+    o_ref, lse_ref = oracle_decode(w, q, k, v)
+    check(o, lse, o_ref.reshape(o.shape), lse_ref.reshape(lse.shape), str(shape))
+
+
+def test_decode_split_invariance():
+    """Different nsplit give the same result (LSE recombination), within tolerance."""
+    w = W.custom(2, 8, 2, 1, 5000, 128, False, seed_index=700, decode=True, nsplit=1)
+    q, k, v = (t.cuda() for t in W.make_inputs(w, "cpu"))
+    o1, l1 = run_decode(w, q, k, v, 1)
+    for ns in (2, 3, 32, 257):
+        o2, l2 = run_decode(w, q, k, v, ns)
+        assert (o1.float() - o2.float()).abs().max().item() < 2e-3
+        assert (l1 - l2).abs().max().item() < 1e-4
+
+
+# ----------------------------------------------------------------------------- boundary
+
+
+def test_errors_are_returned_not_launched():
+    q = torch.zeros(1, 2, 128, 64, dtype=torch.bfloat16, device="cuda")
+    o = torch.zeros_like(q)
+    lse = torch.zeros(1, 2, 128, dtype=torch.float32, device="cuda")
+    with pytest.raises(attn.AttnError) as e:
+        attn.attn_fwd(q.data_ptr() + 2, q, q, o, lse, 1, 2, 2, 128, 128, 64, False, 0.125)
+    assert e.value.status == -2
+    with pytest.raises(attn.AttnError) as e:
+        attn.attn_fwd(q, q, q, o, lse, 1, 2, 2, 128, 128, 96, False, 0.125)
+    assert e.value.status == -3
+    with pytest.raises(attn.AttnError) as e:
+        attn.attn_fwd(q, q, q, o, lse, 1, 2, 2, 128, 128, 64, False, -1.0)
+    assert e.value.status == -3
+    with pytest.raises(attn.AttnError) as e:
+        attn.attn_decode_splitkv(q, q, q, o, lse, 1, 2, 2, 64, 64, 65)
+    assert e.value.status == -3
+    assert torch.count_nonzero(o).item() == 0
+    assert attn.attn_get_device_error() == 0
