@@ -76,6 +76,22 @@ static_assert(sizeof(Misc) <= 4096, "misc region");
 
 __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xFFFFFFFFu, v); }
 
+// Optional event trace (compile with -DATTN_TRACE): clock64 stamps of the
+// pipeline events of the first CTAs, for latency analysis.  Off by default.
+#ifdef ATTN_TRACE
+constexpr int kTraceCtas = 16;
+__device__ unsigned long long g_attn_trace[kTraceCtas * 1024];
+#define ATTN_TRACE_EV(E, t, j)                                                     \
+  do {                                                                            \
+    if (blockIdx.x < kTraceCtas && (j) < 64)                                      \
+      g_attn_trace[blockIdx.x * 1024 + ((E) * 2 + (t)) * 64 + (j)] = clock64();   \
+  } while (0)
+#else
+#define ATTN_TRACE_EV(E, t, j) \
+  do {                         \
+  } while (0)
+#endif
+
 // Wait used only while tearing down after an abort: ignores the abort flag and
 // gives up after a bounded number of polls (each poll suspends briefly), so
 // copies and MMAs already in flight retire before the CTA exits.
@@ -127,6 +143,37 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
       : "memory");
 }
 #undef ATTN_R8
+
+// S = Q K^T over the head dimension: D/16 k-steps of 16 columns; inside a
+// 128-byte swizzle chunk a k-step advances the start address by 32 bytes,
+// the next 64-column chunk starts 128 rows * 128 bytes further.
+template <int KK, int NK>
+__device__ __forceinline__ void issue_s_rec(uint32_t d, uint64_t a0, uint64_t b0, uint32_t idesc) {
+  if constexpr (KK < NK) {
+    constexpr uint32_t off = ((KK >> 2) * (kBM * 128) + (KK & 3) * 32) >> 4;
+    mma_ss_off<off, off>(d, a0, b0, idesc, KK > 0 ? 1u : 0u);
+    issue_s_rec<KK + 1, NK>(d, a0, b0, idesc);
+  }
+}
+template <int D>
+__device__ __forceinline__ void issue_s_steps(uint32_t d, uint64_t a0, uint64_t b0,
+                                              uint32_t idesc) {
+  issue_s_rec<0, D / 16>(d, a0, b0, idesc);
+}
+// O += P V over the keys: 8 k-steps of 16 keys; P packs 2 keys per TMEM
+// column (8 columns per step), V advances 16 rows * 128 bytes per step.
+template <int KK>
+__device__ __forceinline__ void issue_pv_rec(uint32_t d, uint32_t a, uint64_t b0, uint32_t idesc,
+                                             uint32_t acc) {
+  if constexpr (KK < kBN / 16) {
+    mma_ts_off<((KK * 16 * 128) >> 4)>(d, a + KK * 8, b0, idesc, (acc | KK) ? 1u : 0u);
+    issue_pv_rec<KK + 1>(d, a, b0, idesc, acc);
+  }
+}
+__device__ __forceinline__ void issue_pv_steps(uint32_t d, uint32_t a, uint64_t b0, uint32_t idesc,
+                                               uint32_t acc) {
+  issue_pv_rec<0>(d, a, b0, idesc, acc);
+}
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
@@ -207,9 +254,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < n_kv; ++j) {
       if (!warp_all(mbar_wait(&ms.s_full[t], j & 1, abort_flag, p.err, kErrWaitSoftmax, lim)))
         break;
+      if (r == 0) ATTN_TRACE_EV(0, t, j);
       tc_fence_after();
       uint32_t sr[128];
       tmem_ld128(s_addr, sr);
+      if (r == 0) ATTN_TRACE_EV(1, t, j);
       float s[kBN];
 #pragma unroll
       for (int c = 0; c < kBN; ++c) s[c] = __uint_as_float(sr[c]);
@@ -223,15 +272,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (c >= lim_c) s[c] = -CUDART_INF_F;
       }
       {
-        float a0 = s[0], a1 = s[1], a2 = s[2], a3 = s[3];
+        // four independent chains of 3-input max (two new columns per instruction)
+        static_assert(kBN % 8 == 0, "row length");
+        float a0 = fmaxf(s[0], s[1]), a1 = fmaxf(s[2], s[3]);
+        float a2 = fmaxf(s[4], s[5]), a3 = fmaxf(s[6], s[7]);
 #pragma unroll
-        for (int c = 4; c < kBN; c += 4) {
-          a0 = fmaxf(a0, s[c]);
-          a1 = fmaxf(a1, s[c + 1]);
-          a2 = fmaxf(a2, s[c + 2]);
-          a3 = fmaxf(a3, s[c + 3]);
+        for (int c = 8; c < kBN; c += 8) {
+          a0 = max3f(a0, s[c], s[c + 1]);
+          a1 = max3f(a1, s[c + 2], s[c + 3]);
+          a2 = max3f(a2, s[c + 4], s[c + 5]);
+          a3 = max3f(a3, s[c + 6], s[c + 7]);
         }
-        mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
+        mx = max3f(a0, a1, fmaxf(a2, a3));
       }
       // running max in log2 units (scale >= 0, so max commutes with scaling)
       const float m_tile = (mx == -CUDART_INF_F) ? -CUDART_INF_F : mx * p.scale_log2;
@@ -244,6 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ms.alpha[t][r] = alpha;
         mbar_arrive(&ms.stats[t]);
       }
+      if (r == 0) ATTN_TRACE_EV(2, t, j);
       // p = 2^(s*scale*log2e - m), masked entries exactly 0
       const float neg_m = -m;
       float rs0 = 0.f, rs1 = 0.f;
@@ -261,20 +314,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk[c / 2] = pack_bf16x2(p0, p1);
         }
       } else {
+        // packed fp32x2: one FMA and one add per pair of columns
+        const uint64_t scale2 = f32x2(p.scale_log2, p.scale_log2);
+        const uint64_t negm2 = f32x2(neg_m, neg_m);
+        uint64_t acc0 = f32x2(0.f, 0.f), acc1 = acc0;
 #pragma unroll
-        for (int c = 0; c < kBN; c += 2) {
-          const float p0 = ex2_approx(fmaf(s[c], p.scale_log2, neg_m));
-          const float p1 = ex2_approx(fmaf(s[c + 1], p.scale_log2, neg_m));
-          rs0 += p0;
-          rs1 += p1;
+        for (int c = 0; c < kBN; c += 4) {
+          float x0, x1, x2, x3;
+          unpack_f32x2(fma_f32x2(f32x2(s[c], s[c + 1]), scale2, negm2), x0, x1);
+          unpack_f32x2(fma_f32x2(f32x2(s[c + 2], s[c + 3]), scale2, negm2), x2, x3);
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+          acc0 = add_f32x2(acc0, f32x2(p0, p1));
+          acc1 = add_f32x2(acc1, f32x2(p2, p3));
           pk[c / 2] = pack_bf16x2(p0, p1);
+          pk[c / 2 + 1] = pack_bf16x2(p2, p3);
         }
+        float u0, u1, u2, u3;
+        unpack_f32x2(acc0, u0, u1);
+        unpack_f32x2(acc1, u2, u3);
+        rs0 = u0 + u2;
+        rs1 = u1 + u3;
       }
       l = fmaf(l, alpha, rs0 + rs1);
+      if (r == 0) ATTN_TRACE_EV(3, t, j);
       // P (bf16 pairs) over the first 64 columns of S
       tmem_st64(s_addr, pk);
       tc_fence_before();
       mbar_arrive(&ms.p_full[t]);
+      if (r == 0) ATTN_TRACE_EV(4, t, j);
     }
     if (!*abort_flag) {
       ms.m_fin[t][r] = m;
@@ -378,6 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = it % C::kStages;
         const uint32_t ph = static_cast<uint32_t>(it / C::kStages) & 1u;
         if (!mbar_wait(&ms.kv_empty[s], ph ^ 1u, abort_flag, p.err, kErrWaitLoad, lim)) break;
+        ATTN_TRACE_EV(7, it & 1, it >> 1);
         mbar_arrive_expect_tx(&ms.kv_full[s], C::kTileBytes);
         const CUtensorMap* map = (it & 1) ? &p.tmap_v : &p.tmap_k;
         uint8_t* dst = smem + C::kOffKV + s * C::kTileBytes;
@@ -402,70 +471,75 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, kBN, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
-      const uint32_t q_addr = smem_u32(smem + C::kOffQ);
-      const uint32_t kv_addr = smem_u32(smem + C::kOffKV);
+      constexpr uint32_t kTileDesc = C::kTileBytes >> 4;  // one tile in descriptor units
+      // Descriptors are built once; every k-step only adds a constant to the
+      // start-address field, so issuing an MMA costs a couple of instructions.
+      const uint64_t desc_q = sdesc_sw128(smem_u32(smem + C::kOffQ), 16, 1024);
+      const uint64_t desc_k = sdesc_sw128(smem_u32(smem + C::kOffKV), 16, 1024);
+      const uint64_t desc_v = sdesc_sw128(smem_u32(smem + C::kOffKV), kBM * 128, 1024);
       bool ok = mbar_wait(&ms.q_full, 0, abort_flag, p.err, kErrWaitMma, lim);
-      // P_t V_{jv} into O_t
-      auto issue_pv = [&](int t, int jv) -> bool {
+      // S_t = Q_t K^T from the K tile in ring slot `slot`
+      auto issue_s = [&](int t, uint32_t slot) {
+        const uint64_t a0 = desc_q + static_cast<uint32_t>(t) * kTileDesc;
+        const uint64_t b0 = desc_k + slot * kTileDesc;
+        const uint32_t d = tmem + (t ? C::kColS1 : C::kColS0);
+        issue_s_steps<D>(d, a0, b0, idesc_s);
+      };
+      // O_t (+)= P_t V from the V tile in ring slot `slot`; P_t is in TMEM over S_t
+      auto issue_pv = [&](int t, uint32_t slot, uint32_t acc) {
+        const uint64_t b0 = desc_v + slot * kTileDesc;
+        const uint32_t a = tmem + (t ? C::kColS1 : C::kColS0);
+        const uint32_t d = tmem + (t ? C::kColO1 : C::kColO0);
+        issue_pv_steps(d, a, b0, idesc_pv, acc);
+      };
+      // wait for P_t of KV tile jv (and for the correction of O_t, jv > 0)
+      auto wait_p = [&](int t, int jv) -> bool {
         if (!mbar_wait(&ms.p_full[t], jv & 1, abort_flag, p.err, kErrWaitMma, lim)) return false;
+        ATTN_TRACE_EV(5, t, jv);
         if (jv > 0 &&
             !mbar_wait(&ms.o_corr[t], (jv - 1) & 1, abort_flag, p.err, kErrWaitMma, lim))
           return false;
         tc_fence_after();
-        const int itv = 2 * jv + 1;
-        const uint32_t v_base = kv_addr + (itv % C::kStages) * C::kTileBytes;
-        const uint32_t p_tmem = tmem + (t ? C::kColS1 : C::kColS0);
-        const uint32_t o_tmem = tmem + (t ? C::kColO1 : C::kColO0);
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint64_t b = sdesc_sw128(v_base + kk * 16 * 128, kBM * 128, 1024);
-          mma_ts(o_tmem, p_tmem + kk * 8, b, idesc_pv, (jv > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(&ms.o_full[t]);
         return true;
       };
+      constexpr uint32_t kS = C::kStages;  // power of two
+      static_assert((kS & (kS - 1)) == 0, "ring depth must be a power of two");
       for (int j = 0; j < n_kv && ok; ++j) {
-        const int itk = 2 * j;
-        const int sk = itk % C::kStages;
-        ok = mbar_wait(&ms.kv_full[sk], static_cast<uint32_t>(itk / C::kStages) & 1u, abort_flag,
-                       p.err, kErrWaitMma, lim);
+        const uint32_t itk = 2u * j, itv = 2u * j - 1u;
+        const uint32_t sk = itk % kS, sv = itv % kS;
+        ok = mbar_wait(&ms.kv_full[sk], (itk / kS) & 1u, abort_flag, p.err, kErrWaitMma, lim);
+        if (ok && j > 0)
+          ok = mbar_wait(&ms.kv_full[sv], (itv / kS) & 1u, abort_flag, p.err, kErrWaitMma, lim);
         if (!ok) break;
-        int sv = 0;
-        if (j > 0) {
-          const int itv = 2 * (j - 1) + 1;
-          sv = itv % C::kStages;
-          ok = mbar_wait(&ms.kv_full[sv], static_cast<uint32_t>(itv / C::kStages) & 1u,
-                         abort_flag, p.err, kErrWaitMma, lim);
-          if (!ok) break;
-        }
         tc_fence_after();
-        const uint32_t k_base = kv_addr + sk * C::kTileBytes;
         for (int t = 0; t < 2 && ok; ++t) {
-          if (j > 0) ok = issue_pv(t, j - 1);
-          if (!ok) break;
-          const uint32_t q_base_addr = q_addr + t * C::kTileBytes;
-          const uint32_t s_tmem = tmem + (t ? C::kColS1 : C::kColS0);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
-            const uint64_t a = sdesc_sw128(q_base_addr + off, 16, 1024);
-            const uint64_t b = sdesc_sw128(k_base + off, 16, 1024);
-            mma_ss(s_tmem, a, b, idesc_s, kk > 0 ? 1u : 0u);
+          if (j > 0) {
+            ok = wait_p(t, j - 1);
+            if (!ok) break;
+            issue_pv(t, sv, j > 1 ? 1u : 0u);
+            mma_commit(&ms.o_full[t]);
           }
+          issue_s(t, sk);
           mma_commit(&ms.s_full[t]);
+          ATTN_TRACE_EV(6, t, j);
         }
         if (!ok) break;
         mma_commit(&ms.kv_empty[sk]);
         if (j > 0) mma_commit(&ms.kv_empty[sv]);
       }
       if (ok) {
-        const int itv = 2 * (n_kv - 1) + 1;
-        const int sv = itv % C::kStages;
-        ok = mbar_wait(&ms.kv_full[sv], static_cast<uint32_t>(itv / C::kStages) & 1u, abort_flag,
-                       p.err, kErrWaitMma, lim);
+        const uint32_t itv = 2u * (n_kv - 1) + 1u;
+        const uint32_t sv = itv % kS;
+        ok = mbar_wait(&ms.kv_full[sv], (itv / kS) & 1u, abort_flag, p.err, kErrWaitMma, lim);
         if (ok) {
           tc_fence_after();
-          for (int t = 0; t < 2 && ok; ++t) ok = issue_pv(t, n_kv - 1);
+          for (int t = 0; t < 2 && ok; ++t) {
+            ok = wait_p(t, n_kv - 1);
+            if (ok) {
+              issue_pv(t, sv, n_kv > 1 ? 1u : 0u);
+              mma_commit(&ms.o_full[t]);
+            }
+          }
           if (ok) mma_commit(&ms.kv_empty[sv]);
         }
       }

@@ -1,0 +1,63 @@
+"""Run one library kernel on a small named case, for profilers (ncu).
+
+    python -m attention_forward_sm_gb300.profile_case fwd|fwd-causal|decode [--iters N]
+
+Each case keeps every input tensor above the 129 MB L2 but the whole case
+under ~1 GB of device memory, so a multi-pass ncu capture of one launch
+finishes in seconds.  The printed per-launch time is informational only
+(profilers serialise and replay launches); benchmark numbers come from
+bench.py.
+"""
+from __future__ import annotations
+
+import argparse
+
+import torch
+
+from . import binding as attn
+from . import workloads as W
+
+CASES = {
+    # prefill: 4 x 32 heads x 4096 rows x 128: 134 MB per tensor
+    "fwd": W.custom(4, 32, 32, 4096, 4096, 128, False, seed_index=900),
+    "fwd-causal": W.custom(4, 32, 32, 4096, 4096, 128, True, seed_index=901),
+    # decode: 8 x 8 KV heads x 16384 keys x 128: 268 MB per cache
+    "decode": W.custom(8, 32, 8, 1, 16384, 128, False, seed_index=902, decode=True, nsplit=32),
+}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("case", choices=sorted(CASES))
+    ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=2)
+    args = ap.parse_args()
+    w = CASES[args.case]
+    q, k, v = W.make_inputs(w, "cuda")
+    o = torch.empty_like(q)
+    if w.decode:
+        lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device="cuda")
+
+        def call():
+            attn.attn_decode_splitkv(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.Nk, w.D, w.nsplit)
+    else:
+        lse = torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device="cuda")
+
+        def call():
+            attn.attn_fwd(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.D, w.causal, w.scale)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.iters):
+        call()
+    b.record()
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_error() == 0
+    print(f"{args.case}: {w.label()}: {a.elapsed_time(b) / args.iters:.3f} ms per launch "
+          f"(informational)")
+
+
+if __name__ == "__main__":
+    main()
