@@ -215,7 +215,7 @@ def run_reference(args):
     w = W.WORKLOADS["prefill"]
     q, k, v = W.make_inputs(w, "cpu")
     total = args.steps + args.warmup
-    per_step = max(8, min(256, 2048 // total))
+    per_step = max(16, min(1024, 8192 // total))
     for _ in range(args.warmup):
         time_oracle(w, q, k, v, per_step, seed=1)
     secs, flops = 0.0, 0.0
@@ -337,7 +337,7 @@ def run_gpu(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         q_h, k_h, v_h = q.cpu(), k.cpu(), v.cpu()
-        dt, fl, threads, desc = time_oracle(wp, q_h, k_h, v_h, 512)
+        dt, fl, threads, desc = time_oracle(wp, q_h, k_h, v_h, 32768)
         cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                "sample": desc, "seconds": dt}
 

@@ -1,0 +1,77 @@
+"""The C ABI on the host (no GPU needed): the library builds, loads, exports
+every function include/attn.h declares, and rejects bad arguments with the
+documented status codes before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from attention_forward_sm_gb300 import binding as attn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from attention_forward_sm_gb300 import _build
+    _build.build()
+    return attn.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_names():
+    assert set(declared_functions()) <= set(attn.EXPORTED)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    raw = ctypes.CDLL(attn.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(raw, name), name
+
+
+def test_status_strings(lib):
+    for code, name in attn.ATTN_STATUS.items():
+        assert attn.attn_status_string(code).startswith(name)
+    assert "unknown" in attn.attn_status_string(-100)
+
+
+def test_workspace_bytes(lib):
+    assert attn.attn_decode_workspace_bytes(8, 32, 128, 32) == 8 * 32 * 32 * 129 * 4
+    assert attn.attn_decode_workspace_bytes(0, 32, 128, 32) == 0
+
+
+ALIGNED = 0x10000  # never dereferenced: every call below fails validation first
+
+
+@pytest.mark.parametrize("args,status", [
+    ((0, ALIGNED, ALIGNED, ALIGNED, ALIGNED, 1, 2, 2, 8, 8, 64, 0, 0.1), -1),
+    ((ALIGNED,) * 5 + (1, 3, 2, 8, 8, 64, 0, 0.1), -3),          # Hq % Hkv
+    ((ALIGNED,) * 5 + (1, 2, 2, 8, 8, 96, 0, 0.1), -3),          # D
+    ((ALIGNED,) * 5 + (0, 2, 2, 8, 8, 64, 0, 0.1), -3),          # B
+    ((ALIGNED,) * 5 + (1, 2, 2, 0, 8, 64, 0, 0.1), -3),          # Nq
+    ((ALIGNED,) * 5 + (1, 2, 2, 8, 8, 64, 0, -0.5), -3),         # negative scale
+    ((ALIGNED,) * 5 + (1, 2, 2, 8, 8, 64, 0, float("inf")), -3),  # non-finite scale
+    ((ALIGNED + 8,) + (ALIGNED,) * 4 + (1, 2, 2, 8, 8, 64, 0, 0.1), -2),
+])
+def test_fwd_validation(lib, args, status):
+    assert lib.attn_fwd(*args, None) == status
+
+
+@pytest.mark.parametrize("fn", ["attn_decode_splitkv"])
+@pytest.mark.parametrize("args,status", [
+    ((ALIGNED, 0, ALIGNED, ALIGNED, ALIGNED, 1, 4, 2, 16, 128, 4), -1),
+    ((ALIGNED,) * 5 + (1, 4, 2, 16, 128, 17), -3),   # nsplit > Nk
+    ((ALIGNED,) * 5 + (1, 4, 2, 16, 128, 0), -3),    # nsplit < 1
+    ((ALIGNED,) * 5 + (1, 4, 3, 16, 128, 4), -3),    # Hq % Hkv
+    ((ALIGNED,) * 5 + (1, 4, 2, 16, 80, 4), -3),     # D
+    ((ALIGNED,) * 4 + (ALIGNED + 4,) + (1, 4, 2, 16, 128, 4), -2),
+])
+def test_decode_validation(lib, fn, args, status):
+    assert getattr(lib, fn)(*args, None) == status
