@@ -18,10 +18,11 @@ LIB_PATH = os.path.join(PKG, "libattn.so")
 ATTN_STATUS = {
     0: "ATTN_OK", -1: "ATTN_ERR_NULL", -2: "ATTN_ERR_ALIGN", -3: "ATTN_ERR_SHAPE",
     -4: "ATTN_ERR_DEVICE", -5: "ATTN_ERR_LAUNCH", -6: "ATTN_ERR_ALLOC", -7: "ATTN_ERR_TMA",
-    -8: "ATTN_ERR_CUDA",
+    -8: "ATTN_ERR_CUDA", -9: "ATTN_ERR_SCRATCH",
 }
-EXPORTED = ["attn_fwd", "attn_decode_splitkv", "attn_status_string", "attn_get_device_error",
-            "attn_decode_workspace_bytes"]
+EXPORTED = ["attn_fwd", "attn_decode_splitkv", "attn_decode_splitkv_noalloc",
+            "attn_status_string", "attn_get_device_error", "attn_decode_workspace_bytes"]
+NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
 
 _lock = threading.Lock()
 _lib = None
@@ -48,6 +49,8 @@ def load(path: str = LIB_PATH):
         lib.attn_fwd.restype = i
         lib.attn_decode_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, vp]
         lib.attn_decode_splitkv.restype = i
+        lib.attn_decode_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, vp]
+        lib.attn_decode_splitkv_noalloc.restype = i
         lib.attn_status_string.argtypes = [i]
         lib.attn_status_string.restype = ctypes.c_char_p
         lib.attn_get_device_error.argtypes = [vp]
@@ -97,6 +100,17 @@ def attn_decode_splitkv(q, kcache, vcache, o, lse, B, Hq, Hkv, Nk, D, nsplit, st
     _check(load().attn_decode_splitkv(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(o), _ptr(lse),
                                       int(B), int(Hq), int(Hkv), int(Nk), int(D), int(nsplit),
                                       _stream(stream)))
+
+
+def attn_decode_splitkv_noalloc(q, kcache, vcache, o, lse, B, Hq, Hkv, Nk, D, nsplit,
+                                stream=None) -> None:
+    """``attn_decode_splitkv_noalloc`` of include/attn.h: the same decode for
+    callers that cannot allocate device memory during the call; its scratch
+    is a fixed 8 MiB device array shared by all calls on a device (order
+    calls that could overlap on the GPU)."""
+    _check(load().attn_decode_splitkv_noalloc(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(o),
+                                              _ptr(lse), int(B), int(Hq), int(Hkv), int(Nk),
+                                              int(D), int(nsplit), _stream(stream)))
 
 
 def attn_status_string(status: int) -> str:

@@ -106,6 +106,8 @@ const char* attn_status_string(int status) {
     case ATTN_ERR_ALLOC: return "ATTN_ERR_ALLOC: scratch allocation failed";
     case ATTN_ERR_TMA: return "ATTN_ERR_TMA: tensor map encoding failed";
     case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA: a CUDA runtime call failed";
+    case ATTN_ERR_SCRATCH:
+      return "ATTN_ERR_SCRATCH: the problem needs more than the fixed no-allocation scratch";
     default: return "unknown attn status";
   }
 }

@@ -61,7 +61,8 @@ enum attn_status {
   ATTN_ERR_LAUNCH = -5,  /* the kernel launch failed (cudaGetLastError after launch) */
   ATTN_ERR_ALLOC = -6,   /* stream-ordered allocation of the decode scratch failed */
   ATTN_ERR_TMA = -7,     /* cuTensorMapEncodeTiled rejected a tensor view */
-  ATTN_ERR_CUDA = -8     /* another CUDA runtime call failed */
+  ATTN_ERR_CUDA = -8,    /* another CUDA runtime call failed */
+  ATTN_ERR_SCRATCH = -9  /* the problem needs more than the fixed no-allocation scratch */
 };
 
 /* Bits of the device error word (attn_get_device_error). */
@@ -115,6 +116,40 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, i
  */
 int attn_decode_splitkv(const void *q, const void *kcache, const void *vcache, void *o, float *lse,
                         int B, int Hq, int Hkv, int Nk, int D, int nsplit, cudaStream_t stream);
+
+/* Size of the fixed device scratch behind attn_decode_splitkv_noalloc. */
+#define ATTN_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
+
+/*
+ * attn_decode_splitkv_noalloc -- attn_decode_splitkv without any allocation.
+ * (No counterpart on the method's pages: this is a deployment variant.)
+ *
+ * For callers that cannot allocate device memory at call time, e.g. a
+ * serving loop whose device memory is reserved in full by its own allocator
+ * before it starts, or latency-critical code that keeps allocator calls
+ * (which may take locks or wait on other work) off its path.  Arguments,
+ * layouts, numerics and results are those of attn_decode_splitkv; the
+ * partial states live in a fixed array in device memory defined by this
+ * library instead of in stream-ordered allocations.
+ *
+ *   - The array holds ATTN_NOALLOC_SCRATCH_BYTES on every device that loads
+ *     the library, from load until the process exits.
+ *   - A call needs B*Hq*nsplit*(D+1)*4 bytes of it (the decode workload
+ *     B8 Hq32 D128 nsplit32 needs 4.2 MB); a larger problem returns
+ *     ATTN_ERR_SCRATCH and launches nothing.
+ *   - All calls on a device share the one array and it keeps the previous
+ *     call's contents (every element a call reads is first written by that
+ *     same call, so nothing needs clearing).  Two calls whose kernels overlap
+ *     on the GPU -- e.g. on different streams without ordering between them
+ *     -- race on the array and may both return wrong results: order them.
+ *   - The first call on each device does a one-time set-up on the host (it
+ *     looks up the array's device address for the current device); make
+ *     that first call before any stream capture on that device.
+ *   - Calls nothing that allocates or frees memory.
+ */
+int attn_decode_splitkv_noalloc(const void *q, const void *kcache, const void *vcache, void *o,
+                                float *lse, int B, int Hq, int Hkv, int Nk, int D, int nsplit,
+                                cudaStream_t stream);
 
 /* Human-readable name of an ATTN_* status code (static string). */
 const char *attn_status_string(int status);

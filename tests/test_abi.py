@@ -27,7 +27,7 @@ def declared_functions():
 
 
 def test_header_declares_the_binding_names():
-    assert set(declared_functions()) <= set(attn.EXPORTED)
+    assert declared_functions() == sorted(attn.EXPORTED)
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -64,7 +64,7 @@ def test_fwd_validation(lib, args, status):
     assert lib.attn_fwd(*args, None) == status
 
 
-@pytest.mark.parametrize("fn", ["attn_decode_splitkv"])
+@pytest.mark.parametrize("fn", ["attn_decode_splitkv", "attn_decode_splitkv_noalloc"])
 @pytest.mark.parametrize("args,status", [
     ((ALIGNED, 0, ALIGNED, ALIGNED, ALIGNED, 1, 4, 2, 16, 128, 4), -1),
     ((ALIGNED,) * 5 + (1, 4, 2, 16, 128, 17), -3),   # nsplit > Nk
@@ -75,3 +75,8 @@ def test_fwd_validation(lib, args, status):
 ])
 def test_decode_validation(lib, fn, args, status):
     assert getattr(lib, fn)(*args, None) == status
+
+
+def test_noalloc_scratch_limit(lib):
+    # 64*64*64*(128+1)*4 bytes > 8 MiB
+    assert lib.attn_decode_splitkv_noalloc(*(ALIGNED,) * 5, 64, 64, 8, 64, 128, 64, None) == -9
