@@ -89,6 +89,14 @@ int encode_3d(CUtensorMap* map, const void* base, int D, int N, long long BH) {
 }
 
 }  // namespace
+
+unsigned int* device_error_word() {
+  DeviceState* st = nullptr;
+  return device_state(&st) == ATTN_OK ? st->err_word : nullptr;
+}
+
+uint64_t wait_limit_ns() { return kWaitLimitNs; }
+
 }  // namespace attn
 
 using namespace attn;
@@ -177,6 +185,8 @@ int attn_decode_splitkv(const void* q, const void* kcache, const void* vcache, v
   p.D = D;
   p.nsplit = nsplit;
   p.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(D)));
+  p.err = st->err_word;
+  p.wait_limit_ns = kWaitLimitNs;
 
   const size_t o_bytes = static_cast<size_t>(B) * Hq * nsplit * D * sizeof(float);
   const size_t l_bytes = static_cast<size_t>(B) * Hq * nsplit * sizeof(float);

@@ -98,6 +98,9 @@ extern "C" int attn_decode_splitkv_noalloc(const void* q, const void* kcache, co
   p.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(D)));
   // Every partial state is written by the split kernel before the combine
   // kernel reads it, so the scratch needs no clearing between calls.
+  p.err = device_error_word();
+  if (!p.err) return ATTN_ERR_CUDA;
+  p.wait_limit_ns = wait_limit_ns();
   p.ws_o = scratch;
   p.ws_lse = scratch + rows * D;
   if (launch_decode_split(p, stream) != cudaSuccess ||

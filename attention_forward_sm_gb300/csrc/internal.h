@@ -39,7 +39,14 @@ struct DecodeParams {
   float* ws_lse;       // [B, Hq, nsplit] fp32 partial lse (natural log)
   int B, Hq, Hkv, Nk, D, nsplit;
   float scale_log2;
+  unsigned int* err;   // device error word
+  uint64_t wait_limit_ns;
 };
+
+// Device error word of the current device (one-time per-device set-up);
+// nullptr when the current device is unusable.
+unsigned int* device_error_word();
+uint64_t wait_limit_ns();
 
 cudaError_t launch_fwd(const FwdParams& p, cudaStream_t stream);
 size_t fwd_smem_bytes(int D);
