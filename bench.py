@@ -48,6 +48,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-other", action="store_true",
+                    help="skip timing the other prefill workloads (causal, long GQA, tiny)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -331,6 +333,9 @@ def run_gpu(args):
                      "kernels": "decode_split_kernel<128,4> + decode_combine_kernel<128>"},
     }
 
+    other = None
+    if not args.no_other:
+        other = time_other_workloads(attn, W, dev, peaks["bf16_tflops"])
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, attn, W, wp, wd, dev, world)
@@ -356,6 +361,7 @@ def run_gpu(args):
         "gpu_launches": 3 * K,
         "clocks": clocks,
         "prefill_ms_per_call": 1e3 * pf_avg_s,
+        "other_prefill_workloads": other,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -363,6 +369,42 @@ def run_gpu(args):
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def time_other_workloads(attn, W, dev, peak_tflops, calls=3):
+    """CUDA-event time of the other prefill workloads (separate from the step):
+    returns {name: {...}} with TFLOP/s (causal flops halved)."""
+    import torch
+    out = {}
+    for name in ("causal", "long_gqa", "tiny"):
+        w = W.WORKLOADS[name]
+        q, k, v = W.make_inputs(w, dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device=dev)
+        stream = torch.cuda.current_stream(dev)
+
+        def call():
+            attn.attn_fwd(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.D, w.causal, w.scale,
+                          stream.cuda_stream)
+
+        n = calls if name != "tiny" else 50
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            call()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = a.elapsed_time(b) / n
+        tf = w.flops() / (ms * 1e-3) / 1e12
+        out[name] = {"workload": w.label(), "ms_per_call": ms, "tflops": tf,
+                     "frac_of_measured_peak": tf / peak_tflops, "frac_of_nominal_2250": tf / 2250.0,
+                     "calls": n}
+        del q, k, v, o, lse
+        torch.cuda.empty_cache()
+    return out
 
 
 def run_e2e(args, attn, W, wp, wd, dev, world):
