@@ -21,7 +21,9 @@ ATTN_STATUS = {
     -8: "ATTN_ERR_CUDA", -9: "ATTN_ERR_SCRATCH",
 }
 EXPORTED = ["attn_fwd", "attn_decode_splitkv", "attn_decode_splitkv_noalloc",
-            "attn_status_string", "attn_get_device_error", "attn_decode_workspace_bytes"]
+            "attn_status_string", "attn_get_device_error", "attn_decode_workspace_bytes",
+            "attn_selftest_wait_timeout"]
+DEVERR_SELFTEST = 0x10
 NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
 
 _lock = threading.Lock()
@@ -55,6 +57,8 @@ def load(path: str = LIB_PATH):
         lib.attn_status_string.restype = ctypes.c_char_p
         lib.attn_get_device_error.argtypes = [vp]
         lib.attn_get_device_error.restype = i
+        lib.attn_selftest_wait_timeout.argtypes = [ctypes.c_uint, vp]
+        lib.attn_selftest_wait_timeout.restype = i
         lib.attn_decode_workspace_bytes.argtypes = [i, i, i, i]
         lib.attn_decode_workspace_bytes.restype = ctypes.c_longlong
         _lib = lib
@@ -123,6 +127,11 @@ def attn_get_device_error(stream=None) -> int:
     if rc < 0:
         _check(rc)
     return rc
+
+
+def attn_selftest_wait_timeout(limit_us: int, stream=None) -> None:
+    """Launch the bounded-wait self-test (a wait that is meant to run out)."""
+    _check(load().attn_selftest_wait_timeout(int(limit_us), _stream(stream)))
 
 
 def attn_decode_workspace_bytes(B, Hq, D, nsplit) -> int:

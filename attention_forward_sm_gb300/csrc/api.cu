@@ -11,6 +11,7 @@
 
 #include "../../include/attn.h"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace attn {
 
@@ -86,6 +87,21 @@ int encode_3d(CUtensorMap* map, const void* base, int D, int N, long long BH) {
                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_TMA;
+}
+
+// One CTA waits, through the same bounded wait the pipelines use, on an
+// mbarrier that nothing ever arrives at; the wait gives up after `limit_ns`
+// and records `kErrSelfTest` in the device error word.
+__global__ void selftest_wait_kernel(unsigned int* err, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  mbar_wait(&bar, 0, &abort_flag, err, kErrSelfTest, limit_ns);
 }
 
 }  // namespace
@@ -203,6 +219,15 @@ int attn_decode_splitkv(const void* q, const void* kcache, const void* vcache, v
     rc = ATTN_ERR_LAUNCH;
   if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == ATTN_OK) rc = ATTN_ERR_CUDA;
   return rc;
+}
+
+int attn_selftest_wait_timeout(unsigned int limit_us, cudaStream_t stream) {
+  if (limit_us < 1 || limit_us > 1000000) return ATTN_ERR_SHAPE;
+  DeviceState* st = nullptr;
+  if (int rc = device_state(&st)) return rc;
+  selftest_wait_kernel<<<1, 32, 0, stream>>>(st->err_word,
+                                             static_cast<uint64_t>(limit_us) * 1000ull);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
 int attn_get_device_error(cudaStream_t stream) {

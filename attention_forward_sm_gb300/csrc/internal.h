@@ -14,6 +14,7 @@ enum : unsigned int {
   kErrWaitMma = 1u << 1,      // MMA issuer gave up waiting for data / P / correction
   kErrWaitSoftmax = 1u << 2,  // softmax gave up waiting for S
   kErrWaitCorr = 1u << 3,     // correction / epilogue gave up waiting
+  kErrSelfTest = 1u << 4,     // the wait self-test ran out, as intended
 };
 
 // Forward (prefill) launch parameters.  Tensor maps are 3-D views

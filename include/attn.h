@@ -70,6 +70,7 @@ enum attn_status {
 #define ATTN_DEVERR_WAIT_MMA 0x2u     /* MMA issuer gave up waiting for operands */
 #define ATTN_DEVERR_WAIT_SOFTMAX 0x4u /* softmax gave up waiting for scores */
 #define ATTN_DEVERR_WAIT_CORR 0x8u    /* correction / epilogue gave up waiting */
+#define ATTN_DEVERR_SELFTEST 0x10u    /* attn_selftest_wait_timeout ran out, as intended */
 
 /*
  * attn_fwd -- attention forward (prefill).
@@ -158,6 +159,14 @@ const char *attn_status_string(int status);
  * device (ATTN_DEVERR_* bits, 0 when no kernel gave up a wait) and clears
  * it.  Returns a negative ATTN_ERR_* code if a CUDA call fails. */
 int attn_get_device_error(cudaStream_t stream);
+
+/* Failure-detection self-test: launches one CTA that waits, through the same
+ * bounded mbarrier wait the kernels use, on a barrier nothing arrives at.
+ * The wait gives up after limit_us microseconds (1 .. 1e6), sets
+ * ATTN_DEVERR_SELFTEST in the device error word and the kernel exits
+ * normally, leaving the context usable; read the word with
+ * attn_get_device_error().  Returns ATTN_OK once launched. */
+int attn_selftest_wait_timeout(unsigned int limit_us, cudaStream_t stream);
 
 /* Bytes of decode scratch one attn_decode_splitkv call takes. */
 long long attn_decode_workspace_bytes(int B, int Hq, int D, int nsplit);

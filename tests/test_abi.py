@@ -80,3 +80,8 @@ def test_decode_validation(lib, fn, args, status):
 def test_noalloc_scratch_limit(lib):
     # 64*64*64*(128+1)*4 bytes > 8 MiB
     assert lib.attn_decode_splitkv_noalloc(*(ALIGNED,) * 5, 64, 64, 8, 64, 128, 64, None) == -9
+
+
+def test_selftest_limit_validation(lib):
+    assert lib.attn_selftest_wait_timeout(0, None) == -3
+    assert lib.attn_selftest_wait_timeout(2000000, None) == -3
