@@ -22,7 +22,7 @@ ATTN_STATUS = {
 }
 EXPORTED = ["attn_fwd", "attn_decode_splitkv", "attn_decode_splitkv_noalloc",
             "attn_status_string", "attn_get_device_error", "attn_decode_workspace_bytes",
-            "attn_selftest_wait_timeout"]
+            "attn_selftest_wait_timeout", "attn_decode_splitkv_states", "attn_combine_states"]
 DEVERR_SELFTEST = 0x10
 NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
 
@@ -57,6 +57,10 @@ def load(path: str = LIB_PATH):
         lib.attn_status_string.restype = ctypes.c_char_p
         lib.attn_get_device_error.argtypes = [vp]
         lib.attn_get_device_error.restype = i
+        lib.attn_decode_splitkv_states.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, vp]
+        lib.attn_decode_splitkv_states.restype = i
+        lib.attn_combine_states.argtypes = [vp, vp, vp, vp, i, i, i, vp]
+        lib.attn_combine_states.restype = i
         lib.attn_selftest_wait_timeout.argtypes = [ctypes.c_uint, vp]
         lib.attn_selftest_wait_timeout.restype = i
         lib.attn_decode_workspace_bytes.argtypes = [i, i, i, i]
@@ -127,6 +131,20 @@ def attn_get_device_error(stream=None) -> int:
     if rc < 0:
         _check(rc)
     return rc
+
+
+def attn_decode_splitkv_states(q, kcache, vcache, o_state, lse, B, Hq, Hkv, Nk, D, nsplit,
+                               stream=None) -> None:
+    """``attn_decode_splitkv_states`` of include/attn.h (fp32 state output)."""
+    _check(load().attn_decode_splitkv_states(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(o_state),
+                                             _ptr(lse), int(B), int(Hq), int(Hkv), int(Nk),
+                                             int(D), int(nsplit), _stream(stream)))
+
+
+def attn_combine_states(part_o, part_lse, o, lse, rows, nparts, D, stream=None) -> None:
+    """``attn_combine_states`` of include/attn.h."""
+    _check(load().attn_combine_states(_ptr(part_o), _ptr(part_lse), _ptr(o), _ptr(lse), int(rows),
+                                      int(nparts), int(D), _stream(stream)))
 
 
 def attn_selftest_wait_timeout(limit_us: int, stream=None) -> None:

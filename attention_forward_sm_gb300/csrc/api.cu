@@ -221,6 +221,74 @@ int attn_decode_splitkv(const void* q, const void* kcache, const void* vcache, v
   return rc;
 }
 
+int attn_decode_splitkv_states(const void* q, const void* kcache, const void* vcache,
+                               float* o_state, float* lse, int B, int Hq, int Hkv, int Nk, int D,
+                               int nsplit, cudaStream_t stream) {
+  if (!q || !kcache || !vcache || !o_state || !lse) return ATTN_ERR_NULL;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Nk < 1 || Hq % Hkv != 0) return ATTN_ERR_SHAPE;
+  if (D != 64 && D != 128) return ATTN_ERR_SHAPE;
+  if (nsplit < 1 || nsplit > Nk) return ATTN_ERR_SHAPE;
+  if (B > 65535 || Hq > 65535) return ATTN_ERR_SHAPE;
+  if (!decode_supported(Hq / Hkv, D)) return ATTN_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o_state) ||
+      !aligned16(lse))
+    return ATTN_ERR_ALIGN;
+  DeviceState* st = nullptr;
+  if (int rc = device_state(&st)) return rc;
+  DecodeParams p = {};
+  p.q = q;
+  p.k = kcache;
+  p.v = vcache;
+  p.o_state = o_state;
+  p.lse = lse;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Nk = Nk;
+  p.D = D;
+  p.nsplit = nsplit;
+  p.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(D)));
+  p.err = st->err_word;
+  p.wait_limit_ns = kWaitLimitNs;
+  const size_t o_bytes = static_cast<size_t>(B) * Hq * nsplit * D * sizeof(float);
+  const size_t l_bytes = static_cast<size_t>(B) * Hq * nsplit * sizeof(float);
+  void* ws = nullptr;
+  if (cudaMallocAsync(&ws, o_bytes + l_bytes, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_ALLOC;
+  }
+  p.ws_o = static_cast<float*>(ws);
+  p.ws_lse = reinterpret_cast<float*>(static_cast<char*>(ws) + o_bytes);
+  int rc = ATTN_OK;
+  if (launch_decode_split(p, stream) != cudaSuccess ||
+      launch_decode_combine(p, stream) != cudaSuccess)
+    rc = ATTN_ERR_LAUNCH;
+  if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == ATTN_OK) rc = ATTN_ERR_CUDA;
+  return rc;
+}
+
+int attn_combine_states(const float* part_o, const float* part_lse, void* o, float* lse,
+                        int rows, int nparts, int D, cudaStream_t stream) {
+  if (!part_o || !part_lse || !o || !lse) return ATTN_ERR_NULL;
+  if (rows < 1 || nparts < 1 || (D != 64 && D != 128)) return ATTN_ERR_SHAPE;
+  if (!aligned16(part_o) || !aligned16(o)) return ATTN_ERR_ALIGN;
+  DeviceState* st = nullptr;
+  if (int rc = device_state(&st)) return rc;
+  DecodeParams p = {};
+  p.o = o;
+  p.lse = lse;
+  p.ws_o = const_cast<float*>(part_o);
+  p.ws_lse = const_cast<float*>(part_lse);
+  p.B = rows;
+  p.Hq = 1;
+  p.Hkv = 1;
+  p.D = D;
+  p.nsplit = nparts;
+  p.err = st->err_word;
+  p.wait_limit_ns = kWaitLimitNs;
+  return launch_decode_combine(p, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
 int attn_selftest_wait_timeout(unsigned int limit_us, cudaStream_t stream) {
   if (limit_us < 1 || limit_us > 1000000) return ATTN_ERR_SHAPE;
   DeviceState* st = nullptr;

@@ -393,7 +393,10 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeParams p)
   const float* o_in = p.ws_o + row * p.nsplit * D + d;
   for (int c = 0; c < p.nsplit; ++c)
     o = fmaf(ex2_approx((lse_in[c] - L) * kLog2e), o_in[static_cast<size_t>(c) * D], o);
-  static_cast<__nv_bfloat16*>(p.o)[row * D + d] = __float2bfloat16_rn(o);
+  if (p.o_state)
+    p.o_state[row * D + d] = o;  // unrounded state for a further combine
+  else
+    static_cast<__nv_bfloat16*>(p.o)[row * D + d] = __float2bfloat16_rn(o);
   if (d == 0) p.lse[row] = L;
 }
 

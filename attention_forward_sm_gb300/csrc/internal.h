@@ -34,7 +34,8 @@ struct DecodeParams {
   const void* q;       // [B, Hq, D] bf16
   const void* k;       // [B, Hkv, Nk, D] bf16
   const void* v;       // [B, Hkv, Nk, D] bf16
-  void* o;             // [B, Hq, D] bf16
+  void* o;             // [B, Hq, D] bf16 (unless o_state is set)
+  float* o_state;      // optional [B, Hq, D] fp32 output instead of o
   float* lse;          // [B, Hq] fp32
   float* ws_o;         // [B, Hq, nsplit, D] fp32 partial outputs (normalised per chunk)
   float* ws_lse;       // [B, Hq, nsplit] fp32 partial lse (natural log)

@@ -118,6 +118,34 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, i
 int attn_decode_splitkv(const void *q, const void *kcache, const void *vcache, void *o, float *lse,
                         int B, int Hq, int Hkv, int Nk, int D, int nsplit, cudaStream_t stream);
 
+/*
+ * Sequence-parallel decode building blocks (SP FlashDecode, smzdm digest,
+ * section 5): each rank holds a contiguous shard of the key axis, computes
+ * one state per (batch, q head) -- the shard's normalised output and its lse,
+ * [D + 1] numbers -- the ranks exchange the states, and the states are
+ * recombined through their lse weights.  Exchanged volume is independent of
+ * the cache length.
+ *
+ * attn_decode_splitkv_states: attn_decode_splitkv over this rank's cache
+ * shard, with the output kept in fp32 (o_state [B, Hq, D]) so it can be
+ * combined again without an extra rounding; lse [B, Hq] fp32 (natural log).
+ * Same arguments, limits and scratch as attn_decode_splitkv.
+ */
+int attn_decode_splitkv_states(const void *q, const void *kcache, const void *vcache,
+                               float *o_state, float *lse, int B, int Hq, int Hkv, int Nk, int D,
+                               int nsplit, cudaStream_t stream);
+
+/*
+ * attn_combine_states: log-sum-exp combine of nparts partial states per row:
+ *   part_o [rows, nparts, D] fp32 (each normalised by its own softmax sum),
+ *   part_lse [rows, nparts] fp32 (natural log; -inf marks an empty part),
+ *   o [rows, D] bf16 and lse [rows] fp32 written:
+ *   L = ln sum_c exp(lse_c),  O = sum_c exp(lse_c - L) O_c.
+ * Every row needs at least one non-empty part.  D in {64, 128}.
+ */
+int attn_combine_states(const float *part_o, const float *part_lse, void *o, float *lse, int rows,
+                        int nparts, int D, cudaStream_t stream);
+
 /* Size of the fixed device scratch behind attn_decode_splitkv_noalloc. */
 #define ATTN_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
 

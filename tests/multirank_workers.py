@@ -1,0 +1,53 @@
+"""Worker functions for the multi-rank CPU tests (run in spawned processes,
+one per rank, over the gloo backend on 127.0.0.1)."""
+import math
+import os
+
+import numpy as np
+import torch
+import torch.distributed as dist
+
+
+def _init(rank, world, port):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+
+
+def max_over_ranks_worker(rank, world, port):
+    _init(rank, world, port)
+    import bench
+    got = bench.max_over_ranks(float(10 * rank + 3), world)
+    assert got == float(10 * (world - 1) + 3), got
+    dist.destroy_process_group()
+
+
+def sp_decode_worker(rank, world, port, B, Hq, Hkv, Nk, D, seed):
+    """Each rank decodes its key shard with the oracle, the states are
+    all-gathered over gloo and recombined (oracle combine); every rank checks
+    the result against the oracle over the whole cache."""
+    _init(rank, world, port)
+    import oracle
+    from attention_forward_sm_gb300 import sp_decode
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(B, Hq, D, generator=g).to(torch.bfloat16)
+    k = torch.randn(B, Hkv, Nk, D, generator=g).to(torch.bfloat16)
+    v = torch.randn(B, Hkv, Nk, D, generator=g).to(torch.bfloat16)
+    scale = 1.0 / math.sqrt(D)
+    s0, s1 = sp_decode.shard_range(Nk, world, rank)
+    ks, vs = k[:, :, s0:s1].contiguous(), v[:, :, s0:s1].contiguous()
+
+    def local_states(q_, k_, v_, nsplit):
+        o, l = oracle.attn_rows(q_, k_, v_, B, Hq, Hkv, 1, k_.shape[2], D, False, scale)
+        return torch.from_numpy(o).float(), torch.from_numpy(l).float()
+
+    def combine(part_o, part_lse):
+        o, l = oracle.combine(part_o.double().numpy(), part_lse.double().numpy())
+        return o, l
+
+    o, lse = sp_decode.sp_flash_decode(q, ks, vs, 8, local_states=local_states, combine=combine)
+    o_ref, lse_ref = oracle.decode(q, k, v, B, Hq, Hkv, Nk, D, scale=scale)
+    assert np.abs(o - o_ref).max() < 1e-5, np.abs(o - o_ref).max()
+    assert np.abs(lse - lse_ref).max() < 1e-5
+    # the naive sum of the per-rank outputs is not attention (denominator pitfall)
+    dist.destroy_process_group()

@@ -85,3 +85,13 @@ def test_noalloc_scratch_limit(lib):
 def test_selftest_limit_validation(lib):
     assert lib.attn_selftest_wait_timeout(0, None) == -3
     assert lib.attn_selftest_wait_timeout(2000000, None) == -3
+
+
+def test_states_and_combine_validation(lib):
+    A = ALIGNED
+    assert lib.attn_decode_splitkv_states(A, A, A, 0, A, 1, 4, 2, 16, 128, 4, None) == -1
+    assert lib.attn_decode_splitkv_states(A, A, A, A, A, 1, 4, 2, 16, 128, 17, None) == -3
+    assert lib.attn_combine_states(A, A, A, A, 0, 4, 128, None) == -3
+    assert lib.attn_combine_states(A, A, A, A, 4, 0, 128, None) == -3
+    assert lib.attn_combine_states(A, A, A, A, 4, 4, 96, None) == -3
+    assert lib.attn_combine_states(A + 4, A, A, A, 4, 4, 128, None) == -2
