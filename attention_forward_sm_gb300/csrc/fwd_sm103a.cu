@@ -41,9 +41,13 @@ namespace {
 
 constexpr int kBM = 128;          // query rows per tile
 constexpr int kBN = 128;          // keys per K/V tile
-constexpr int kThreads = 512;     // 16 warps
-constexpr int kWarpLoad = 12;
-constexpr int kWarpMma = 13;
+constexpr int kThreads = 640;     // 20 warps: 16 softmax/epilogue + load, MMA, 2 idle
+constexpr int kWarpLoad = 16;
+constexpr int kWarpMma = 17;
+// setmaxnreg split of the 61440 registers the launch gets (640 threads x 96):
+// 4 softmax warpgroups + 1 warpgroup for load / MMA / idle warps.
+constexpr uint32_t kRegSoftmax = 112, kRegOther = 32;
+static_assert(4 * 128 * kRegSoftmax + 128 * kRegOther <= 640 * 96, "register split");
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max rises > 2^8
 
 template <int D>
@@ -63,14 +67,13 @@ struct Cfg {
 
 struct Misc {
   uint64_t q_full;
-  uint64_t s_full[2], p_full[2], o_full[2], o_corr[2], stats[2], fin_full[2];
+  uint64_t s_full[2];     // S_t = Q_t K^T in TMEM (MMA commit)
+  uint64_t p_full[2];     // P_t in TMEM (one arrival per softmax warp of the tile)
+  uint64_t o_done[2];     // every MMA of O_t retired (single phase)
   uint64_t mma_done;
   uint64_t kv_full[8], kv_empty[8];
   uint32_t tmem_base;
   int abort_flag;
-  float alpha[2][kBM];
-  float m_fin[2][kBM];
-  float l_fin[2][kBM];
 };
 static_assert(sizeof(Misc) <= 4096, "misc region");
 
@@ -210,11 +213,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&ms.q_full, 1);
     for (int t = 0; t < 2; ++t) {
       mbar_init(&ms.s_full[t], 1);
-      mbar_init(&ms.p_full[t], kBM);
-      mbar_init(&ms.o_full[t], 1);
-      mbar_init(&ms.o_corr[t], kBM);
-      mbar_init(&ms.stats[t], kBM);
-      mbar_init(&ms.fin_full[t], kBM);
+      mbar_init(&ms.p_full[t], 8);
+      mbar_init(&ms.o_done[t], 1);
     }
     mbar_init(&ms.mma_done, 1);
     for (int s = 0; s < C::kStages; ++s) {
@@ -238,52 +238,65 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = ms.tmem_base;
   const uint64_t lim = p.wait_limit_ns;
 
-  if (warp < 8) {
+  if (warp < 16) {
     // =====================================================================
-    // softmax warpgroup t: thread = query row r of tile t
+    // softmax + epilogue: warps 8t .. 8t + 7 serve query tile t.  Two warps
+    // share each 32-lane TMEM quarter (16 rows each), and the two threads
+    // t and t + 16 of a warp share one row: thread half c holds key columns
+    // [64c, 64c + 64) of the row.  Per SMSP that puts two warps of a tile on
+    // the exponentials at once, and the row max needs one shuffle.
     // =====================================================================
-    reg_alloc<184>();
-    const int t = warp >> 2;
-    const int r = (warp & 3) * 32 + lane;
+    reg_alloc<kRegSoftmax>();
+    const int t = warp >> 3;
+    const int lbase = (warp & 3) * 32 + ((warp >> 2) & 1) * 16;  // first TMEM lane of the warp
+    const int r = lbase + (lane & 15);                              // row within the tile
+    const int c = lane >> 4;                                        // column half of the row
     const int row = q_base + t * kBM + r;
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(lbase) << 16);
     const uint32_t s_addr = lane_addr + (t ? C::kColS1 : C::kColS0);
+    const uint32_t o_addr = lane_addr + (t ? C::kColO1 : C::kColO0);
     const int tile_row0 = q_base + t * kBM;
     const int vis = p.causal ? min(row + 1, p.Nk) : p.Nk;  // keys [0, vis) visible
-    float m = -CUDART_INF_F, l = 0.f;
+    const bool tracer = (warp & 7) == 0 && lane == 0;
+    float m = -CUDART_INF_F, l = 0.f;  // l: sum over this thread's half of the row
+    bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
-      if (!warp_all(mbar_wait(&ms.s_full[t], j & 1, abort_flag, p.err, kErrWaitSoftmax, lim)))
+      if (!warp_all(mbar_wait(&ms.s_full[t], j & 1, abort_flag, p.err, kErrWaitSoftmax, lim))) {
+        ok = false;
         break;
-      if (r == 0) ATTN_TRACE_EV(0, t, j);
+      }
+      if (tracer) ATTN_TRACE_EV(0, t, j);
       tc_fence_after();
-      uint32_t sr[128];
-      tmem_ld128(s_addr, sr);
-      if (r == 0) ATTN_TRACE_EV(1, t, j);
-      float s[kBN];
+      float s[64];
+      {
+        uint32_t sr[64];
+        tmem_ld_pair64<64>(s_addr, sr);
 #pragma unroll
-      for (int c = 0; c < kBN; ++c) s[c] = __uint_as_float(sr[c]);
-      const int kb = j * kBN;
-      const bool need_mask = (kb + kBN > p.Nk) || (p.causal && kb + kBN - 1 > tile_row0);
-      float mx;
+        for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(sr[i]);
+      }
+      if (tracer) ATTN_TRACE_EV(1, t, j);
+      const int kb = j * kBN + c * 64;  // key index of this thread's first column
+      const bool need_mask =
+          (j * kBN + kBN > p.Nk) || (p.causal && j * kBN + kBN - 1 > tile_row0);
       if (need_mask) {
         const int lim_c = vis - kb;  // columns [0, lim_c) valid
 #pragma unroll
-        for (int c = 0; c < kBN; ++c)
-          if (c >= lim_c) s[c] = -CUDART_INF_F;
+        for (int i = 0; i < 64; ++i)
+          if (i >= lim_c) s[i] = -CUDART_INF_F;
       }
+      float mx;
       {
-        // four independent chains of 3-input max (two new columns per instruction)
-        static_assert(kBN % 8 == 0, "row length");
         float a0 = fmaxf(s[0], s[1]), a1 = fmaxf(s[2], s[3]);
         float a2 = fmaxf(s[4], s[5]), a3 = fmaxf(s[6], s[7]);
 #pragma unroll
-        for (int c = 8; c < kBN; c += 8) {
-          a0 = max3f(a0, s[c], s[c + 1]);
-          a1 = max3f(a1, s[c + 2], s[c + 3]);
-          a2 = max3f(a2, s[c + 4], s[c + 5]);
-          a3 = max3f(a3, s[c + 6], s[c + 7]);
+        for (int i = 8; i < 64; i += 8) {
+          a0 = max3f(a0, s[i], s[i + 1]);
+          a1 = max3f(a1, s[i + 2], s[i + 3]);
+          a2 = max3f(a2, s[i + 4], s[i + 5]);
+          a3 = max3f(a3, s[i + 6], s[i + 7]);
         }
         mx = max3f(a0, a1, fmaxf(a2, a3));
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));  // the row's other half
       }
       // running max in log2 units (scale >= 0, so max commutes with scaling)
       const float m_tile = (mx == -CUDART_INF_F) ? -CUDART_INF_F : mx * p.scale_log2;
@@ -292,147 +305,120 @@ __global__ void __launch_bounds__(kThreads, 1)
         alpha = ex2_approx(m - m_tile);  // 0 on the first tile
         m = m_tile;
       }
-      if (j > 0) {
-        ms.alpha[t][r] = alpha;
-        mbar_arrive(&ms.stats[t]);
-      }
-      if (r == 0) ATTN_TRACE_EV(2, t, j);
+      if (tracer) ATTN_TRACE_EV(2, t, j);
       // p = 2^(s*scale*log2e - m), masked entries exactly 0
       const float neg_m = -m;
-      float rs0 = 0.f, rs1 = 0.f;
-      uint32_t pk[64];
+      float rsum;
+      uint32_t pk[32];
       if (need_mask) {
+        float r0 = 0.f, r1 = 0.f;
 #pragma unroll
-        for (int c = 0; c < kBN; c += 2) {
+        for (int i = 0; i < 64; i += 2) {
           const float p0 =
-              (s[c] == -CUDART_INF_F) ? 0.f : ex2_approx(fmaf(s[c], p.scale_log2, neg_m));
-          const float p1 = (s[c + 1] == -CUDART_INF_F)
+              (s[i] == -CUDART_INF_F) ? 0.f : ex2_approx(fmaf(s[i], p.scale_log2, neg_m));
+          const float p1 = (s[i + 1] == -CUDART_INF_F)
                                ? 0.f
-                               : ex2_approx(fmaf(s[c + 1], p.scale_log2, neg_m));
-          rs0 += p0;
-          rs1 += p1;
-          pk[c / 2] = pack_bf16x2(p0, p1);
+                               : ex2_approx(fmaf(s[i + 1], p.scale_log2, neg_m));
+          r0 += p0;
+          r1 += p1;
+          pk[i / 2] = pack_bf16x2(p0, p1);
         }
+        rsum = r0 + r1;
       } else {
         // packed fp32x2: one FMA and one add per pair of columns
         const uint64_t scale2 = f32x2(p.scale_log2, p.scale_log2);
         const uint64_t negm2 = f32x2(neg_m, neg_m);
         uint64_t acc0 = f32x2(0.f, 0.f), acc1 = acc0;
 #pragma unroll
-        for (int c = 0; c < kBN; c += 4) {
+        for (int i = 0; i < 64; i += 4) {
           float x0, x1, x2, x3;
-          unpack_f32x2(fma_f32x2(f32x2(s[c], s[c + 1]), scale2, negm2), x0, x1);
-          unpack_f32x2(fma_f32x2(f32x2(s[c + 2], s[c + 3]), scale2, negm2), x2, x3);
+          unpack_f32x2(fma_f32x2(f32x2(s[i], s[i + 1]), scale2, negm2), x0, x1);
+          unpack_f32x2(fma_f32x2(f32x2(s[i + 2], s[i + 3]), scale2, negm2), x2, x3);
           const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
           const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
           acc0 = add_f32x2(acc0, f32x2(p0, p1));
           acc1 = add_f32x2(acc1, f32x2(p2, p3));
-          pk[c / 2] = pack_bf16x2(p0, p1);
-          pk[c / 2 + 1] = pack_bf16x2(p2, p3);
+          pk[i / 2] = pack_bf16x2(p0, p1);
+          pk[i / 2 + 1] = pack_bf16x2(p2, p3);
         }
-        float u0, u1, u2, u3;
-        unpack_f32x2(acc0, u0, u1);
-        unpack_f32x2(acc1, u2, u3);
-        rs0 = u0 + u2;
-        rs1 = u1 + u3;
+        float u0, u1;
+        unpack_f32x2(add_f32x2(acc0, acc1), u0, u1);
+        rsum = u0 + u1;
       }
-      l = fmaf(l, alpha, rs0 + rs1);
-      if (r == 0) ATTN_TRACE_EV(3, t, j);
-      // P (bf16 pairs) over the first 64 columns of S
-      tmem_st64(s_addr, pk);
-      tc_fence_before();
-      mbar_arrive(&ms.p_full[t]);
-      if (r == 0) ATTN_TRACE_EV(4, t, j);
-    }
-    if (!*abort_flag) {
-      ms.m_fin[t][r] = m;
-      ms.l_fin[t][r] = l;
-      mbar_arrive(&ms.fin_full[t]);
-    }
-  } else if (warp < 12) {
-    // =====================================================================
-    // correction + epilogue warpgroup: thread = row r of both tiles
-    // =====================================================================
-    reg_dealloc<88>();
-    const int r = (warp & 3) * 32 + lane;
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    bool ok = true;
-    for (int j = 1; j < n_kv && ok; ++j) {
-      for (int t = 0; t < 2 && ok; ++t) {
-        ok = warp_all(
-            mbar_wait(&ms.stats[t], (j - 1) & 1, abort_flag, p.err, kErrWaitCorr, lim));
-        if (!ok) break;
-        const float a = ms.alpha[t][r];
-        if (__any_sync(0xFFFFFFFFu, a != 1.f)) {
-          ok = warp_all(
-              mbar_wait(&ms.o_full[t], (j - 1) & 1, abort_flag, p.err, kErrWaitCorr, lim));
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t o_addr = lane_addr + (t ? C::kColO1 : C::kColO0);
+      l = fmaf(l, alpha, rsum);
+      if (tracer) ATTN_TRACE_EV(3, t, j);
+      // Rescale O_t when a row's max rose past the threshold.  Every P*V of KV
+      // tiles < j has retired: it was issued before S_t(j), whose completion
+      // woke this warp.  The P*V of tile j waits for p_full below.  Thread half
+      // c owns O columns [c*D/2, (c+1)*D/2) of its row.
+      if (j > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.f)) {
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t v[32];
-            tmem_ld32(o_addr + c * 32, v);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * a);
-            tmem_st32(o_addr + c * 32, v);
-          }
-          tmem_st_wait();
-        }
-        tc_fence_before();
-        mbar_arrive(&ms.o_corr[t]);
-      }
-    }
-    // epilogue: O / l -> bf16 -> swizzled smem (the tile's Q buffer) -> TMA store
-    for (int t = 0; t < 2; ++t) {
-      bool good = ok && warp_all(mbar_wait(&ms.fin_full[t], 0, abort_flag, p.err,
-                                           kErrWaitCorr, lim));
-      good = good && warp_all(mbar_wait(&ms.o_full[t], (n_kv - 1) & 1, abort_flag, p.err,
-                                        kErrWaitCorr, lim));
-      uint8_t* stage = smem + C::kOffQ + t * C::kTileBytes;
-      if (good) {
-        tc_fence_after();
-        const float mrow = ms.m_fin[t][r];
-        const float lrow = ms.l_fin[t][r];
-        const float inv = 1.f / lrow;
-        const uint32_t o_addr = lane_addr + (t ? C::kColO1 : C::kColO0);
-        const uint32_t stage_row = smem_u32(stage) + r * 128;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int k = 0; k < D / 64; ++k) {
           uint32_t v[32];
-          tmem_ld32(o_addr + c * 32, v);
-          uint32_t w[16];
+          tmem_ld_pair32<D / 2>(o_addr + k * 32, v);
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            w[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * inv, __uint_as_float(v[2 * i + 1]) * inv);
-          const uint32_t chunk_base = stage_row + (c >> 1) * (kBM * 128);
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            const int gran = (c & 1) * 4 + g;
-            const uint32_t addr = chunk_base + ((gran ^ (r & 7)) << 4);
-            st_shared_v4(addr, w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
-          }
+          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+          tmem_st_pair32<D / 2>(o_addr + k * 32, v);
         }
-        const int row = q_base + t * kBM + r;
-        if (row < p.Nq)
-          p.lse[static_cast<size_t>(bh) * p.Nq + row] =
-              (mrow + __log2f(lrow)) * 0.69314718055994530942f;
+        tmem_st_wait();
       }
-      fence_proxy_async_smem();
-      named_bar_sync(1, 128);
-      if (warp == 8 && lane == 0 && !*abort_flag && q_base + t * kBM < p.Nq) {
+      // P (bf16 pairs) over the first 64 columns of S: this half's 32 columns
+      tmem_st_pair32<32>(s_addr, pk);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ms.p_full[t]);
+      if (tracer) ATTN_TRACE_EV(4, t, j);
+    }
+    // ---- epilogue of tile t: O / l -> bf16 -> swizzled smem (the tile's Q
+    // buffer) -> TMA store; LSE.  Every warp of the tile reaches the named
+    // barrier exactly once, also after an abort.
+    const float l_row = l + __shfl_xor_sync(0xFFFFFFFFu, l, 16);
+    const bool good =
+        ok && warp_all(mbar_wait(&ms.o_done[t], 0, abort_flag, p.err, kErrWaitCorr, lim));
+    uint8_t* stage = smem + C::kOffQ + t * C::kTileBytes;
+    if (good) {
+      tc_fence_after();
+      const float inv = 1.f / l_row;
+      const uint32_t stage_row = smem_u32(stage) + r * 128;
+#pragma unroll
+      for (int k = 0; k < D / 64; ++k) {
+        // columns c*D/2 + [32k, 32k + 32) of the row
+        uint32_t v[32];
+        tmem_ld_pair32<D / 2>(o_addr + k * 32, v);
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          w[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * inv, __uint_as_float(v[2 * i + 1]) * inv);
+        const int col0 = c * (D / 2) + 32 * k;  // first of the 32 columns
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int col = col0 + 8 * g;               // 8 bf16 = one 16-byte granule
+          const int chunk = col >> 6, gran = (col & 63) >> 3;
+          const uint32_t addr = stage_row + chunk * (kBM * 128) + ((gran ^ (r & 7)) << 4);
+          st_shared_v4(addr, w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
+        }
+      }
+      if (c == 0 && row < p.Nq)
+        p.lse[static_cast<size_t>(bh) * p.Nq + row] =
+            (m + __log2f(l_row)) * 0.69314718055994530942f;
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(1 + t, 256);
+    if ((warp & 7) == 0 && lane == 0) {
+      if (!*abort_flag && q_base + t * kBM < p.Nq) {
 #pragma unroll
         for (int ch = 0; ch < C::kChunks; ++ch)
           tma_store_3d(&p.tmap_o, stage + ch * (kBM * 128), ch * 64, q_base + t * kBM, bh);
         tma_store_commit();
       }
+      tma_store_wait_all0();
     }
-    if (warp == 8 && lane == 0) tma_store_wait_all0();
   } else if (warp == kWarpLoad) {
     // =====================================================================
     // TMA loader: Q tiles once, then K_j, V_j through the ring
     // =====================================================================
-    reg_dealloc<56>();
+    reg_dealloc<kRegOther>();
     if (lane == 0) {
       const uint64_t pol_q = l2_policy_evict_first();
       const uint64_t pol_kv = l2_policy_evict_last();
@@ -467,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // =====================================================================
     // MMA issuer (one thread): S_t = Q_t K_j^T, O_t += P_t V_j
     // =====================================================================
-    reg_dealloc<56>();
+    reg_dealloc<kRegOther>();
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, kBN, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
@@ -492,13 +478,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d = tmem + (t ? C::kColO1 : C::kColO0);
         issue_pv_steps(d, a, b0, idesc_pv, acc);
       };
-      // wait for P_t of KV tile jv (and for the correction of O_t, jv > 0)
+      // wait for P_t of KV tile jv (O_t is already rescaled when it arrives)
       auto wait_p = [&](int t, int jv) -> bool {
         if (!mbar_wait(&ms.p_full[t], jv & 1, abort_flag, p.err, kErrWaitMma, lim)) return false;
         ATTN_TRACE_EV(5, t, jv);
-        if (jv > 0 &&
-            !mbar_wait(&ms.o_corr[t], (jv - 1) & 1, abort_flag, p.err, kErrWaitMma, lim))
-          return false;
         tc_fence_after();
         return true;
       };
@@ -517,7 +500,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = wait_p(t, j - 1);
             if (!ok) break;
             issue_pv(t, sv, j > 1 ? 1u : 0u);
-            mma_commit(&ms.o_full[t]);
           }
           issue_s(t, sk);
           mma_commit(&ms.s_full[t]);
@@ -537,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = wait_p(t, n_kv - 1);
             if (ok) {
               issue_pv(t, sv, n_kv > 1 ? 1u : 0u);
-              mma_commit(&ms.o_full[t]);
+              mma_commit(&ms.o_done[t]);
             }
           }
           if (ok) mma_commit(&ms.kv_empty[sv]);
@@ -548,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain_wait(&ms.mma_done, 0);
     }
   } else {
-    reg_dealloc<56>();
+    reg_dealloc<kRegOther>();
   }
 
   tc_fence_before();
