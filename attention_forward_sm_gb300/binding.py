@@ -22,7 +22,8 @@ ATTN_STATUS = {
 }
 EXPORTED = ["attn_fwd", "attn_decode_splitkv", "attn_decode_splitkv_noalloc",
             "attn_status_string", "attn_get_device_error", "attn_decode_workspace_bytes",
-            "attn_selftest_wait_timeout", "attn_decode_splitkv_states", "attn_combine_states"]
+            "attn_selftest_wait_timeout", "attn_decode_splitkv_states", "attn_combine_states",
+            "attn_decode_graph_create", "attn_decode_graph_launch", "attn_decode_graph_destroy"]
 DEVERR_SELFTEST = 0x10
 NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
 
@@ -63,6 +64,13 @@ def load(path: str = LIB_PATH):
         lib.attn_combine_states.restype = i
         lib.attn_selftest_wait_timeout.argtypes = [ctypes.c_uint, vp]
         lib.attn_selftest_wait_timeout.restype = i
+        lib.attn_decode_graph_create.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i,
+                                                 ctypes.POINTER(vp)]
+        lib.attn_decode_graph_create.restype = i
+        lib.attn_decode_graph_launch.argtypes = [vp, vp]
+        lib.attn_decode_graph_launch.restype = i
+        lib.attn_decode_graph_destroy.argtypes = [vp]
+        lib.attn_decode_graph_destroy.restype = i
         lib.attn_decode_workspace_bytes.argtypes = [i, i, i, i]
         lib.attn_decode_workspace_bytes.restype = ctypes.c_longlong
         _lib = lib
@@ -152,6 +160,27 @@ def attn_selftest_wait_timeout(limit_us: int, stream=None) -> None:
     _check(load().attn_selftest_wait_timeout(int(limit_us), _stream(stream)))
 
 
+def attn_decode_graph_create(q, kcache, vcache, o, lse, B, Hq, Hkv, Nk, D, nsplit) -> int:
+    """``attn_decode_graph_create`` of include/attn.h; returns the handle (an
+    integer).  The buffers are bound by address until the handle is
+    destroyed: keep the tensors alive."""
+    h = ctypes.c_void_p()
+    _check(load().attn_decode_graph_create(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(o),
+                                           _ptr(lse), int(B), int(Hq), int(Hkv), int(Nk), int(D),
+                                           int(nsplit), ctypes.byref(h)))
+    return int(h.value)
+
+
+def attn_decode_graph_launch(handle: int, stream=None) -> None:
+    """``attn_decode_graph_launch`` of include/attn.h: replay one decode step."""
+    _check(load().attn_decode_graph_launch(handle or None, _stream(stream)))
+
+
+def attn_decode_graph_destroy(handle: int) -> None:
+    """``attn_decode_graph_destroy`` of include/attn.h."""
+    _check(load().attn_decode_graph_destroy(handle or None))
+
+
 def attn_decode_workspace_bytes(B, Hq, D, nsplit) -> int:
     return int(load().attn_decode_workspace_bytes(int(B), int(Hq), int(D), int(nsplit)))
 
@@ -171,6 +200,38 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, stream=No
     lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
     attn_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, causal, scale, stream)
     return o, lse
+
+
+class DecodeGraph:
+    """One decode step captured as a CUDA graph for fixed q / cache / output
+    tensors (held here, so their addresses stay valid); ``replay()`` runs the
+    step on the buffers' current contents."""
+
+    def __init__(self, q, kcache, vcache, nsplit: int):
+        import torch
+        self.handle = 0
+        B, Hq, D = q.shape
+        Hkv, Nk = kcache.shape[1], kcache.shape[2]
+        self.q, self.kcache, self.vcache = q, kcache, vcache
+        self.o = torch.empty_like(q)
+        self.lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+        self.handle = attn_decode_graph_create(q, kcache, vcache, self.o, self.lse, B, Hq, Hkv,
+                                               Nk, D, nsplit)
+
+    def replay(self, stream=None):
+        attn_decode_graph_launch(self.handle, stream)
+        return self.o, self.lse
+
+    def close(self):
+        if self.handle:
+            h, self.handle = self.handle, 0
+            attn_decode_graph_destroy(h)
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def decode(q, kcache, vcache, nsplit: int, stream=None):

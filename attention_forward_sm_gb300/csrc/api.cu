@@ -113,6 +113,48 @@ unsigned int* device_error_word() {
 
 uint64_t wait_limit_ns() { return kWaitLimitNs; }
 
+int decode_prepare(const void* q, const void* kcache, const void* vcache, void* o, float* o_state,
+                   float* lse, int B, int Hq, int Hkv, int Nk, int D, int nsplit,
+                   DecodeParams* p) {
+  if (!q || !kcache || !vcache || !(o || o_state) || !lse) return ATTN_ERR_NULL;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Nk < 1 || Hq % Hkv != 0) return ATTN_ERR_SHAPE;
+  if (D != 64 && D != 128) return ATTN_ERR_SHAPE;
+  if (nsplit < 1 || nsplit > Nk) return ATTN_ERR_SHAPE;
+  if (B > 65535 || Hq > 65535) return ATTN_ERR_SHAPE;
+  if (!decode_supported(Hq / Hkv, D)) return ATTN_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o) ||
+      !aligned16(o_state) || !aligned16(lse))
+    return ATTN_ERR_ALIGN;
+  *p = DecodeParams{};
+  p->q = q;
+  p->k = kcache;
+  p->v = vcache;
+  p->o = o;
+  p->o_state = o_state;
+  p->lse = lse;
+  p->B = B;
+  p->Hq = Hq;
+  p->Hkv = Hkv;
+  p->Nk = Nk;
+  p->D = D;
+  p->nsplit = nsplit;
+  p->scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(D)));
+  p->wait_limit_ns = kWaitLimitNs;
+  return ATTN_OK;
+}
+
+int decode_bind_device(DecodeParams* p) {
+  DeviceState* st = nullptr;
+  if (int rc = device_state(&st)) return rc;
+  p->err = st->err_word;
+  return ATTN_OK;
+}
+
+size_t decode_scratch_bytes(const DecodeParams& p, size_t* o_bytes) {
+  *o_bytes = static_cast<size_t>(p.B) * p.Hq * p.nsplit * p.D * sizeof(float);
+  return *o_bytes + static_cast<size_t>(p.B) * p.Hq * p.nsplit * sizeof(float);
+}
+
 }  // namespace attn
 
 using namespace attn;
@@ -174,40 +216,13 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   return ATTN_OK;
 }
 
-int attn_decode_splitkv(const void* q, const void* kcache, const void* vcache, void* o, float* lse,
-                        int B, int Hq, int Hkv, int Nk, int D, int nsplit, cudaStream_t stream) {
-  if (!q || !kcache || !vcache || !o || !lse) return ATTN_ERR_NULL;
-  if (B < 1 || Hq < 1 || Hkv < 1 || Nk < 1 || Hq % Hkv != 0) return ATTN_ERR_SHAPE;
-  if (D != 64 && D != 128) return ATTN_ERR_SHAPE;
-  if (nsplit < 1 || nsplit > Nk) return ATTN_ERR_SHAPE;
-  if (B > 65535 || Hq > 65535) return ATTN_ERR_SHAPE;
-  if (!decode_supported(Hq / Hkv, D)) return ATTN_ERR_SHAPE;
-  if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o) ||
-      !aligned16(lse))
-    return ATTN_ERR_ALIGN;
-  DeviceState* st = nullptr;
-  if (int rc = device_state(&st)) return rc;
-
-  DecodeParams p = {};
-  p.q = q;
-  p.k = kcache;
-  p.v = vcache;
-  p.o = o;
-  p.lse = lse;
-  p.B = B;
-  p.Hq = Hq;
-  p.Hkv = Hkv;
-  p.Nk = Nk;
-  p.D = D;
-  p.nsplit = nsplit;
-  p.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(D)));
-  p.err = st->err_word;
-  p.wait_limit_ns = kWaitLimitNs;
-
-  const size_t o_bytes = static_cast<size_t>(B) * Hq * nsplit * D * sizeof(float);
-  const size_t l_bytes = static_cast<size_t>(B) * Hq * nsplit * sizeof(float);
+// Split + combine with stream-ordered scratch for the partial states.
+static int decode_with_scratch(DecodeParams& p, cudaStream_t stream) {
+  if (int rc = decode_bind_device(&p)) return rc;
+  size_t o_bytes = 0;
+  const size_t bytes = decode_scratch_bytes(p, &o_bytes);
   void* ws = nullptr;
-  if (cudaMallocAsync(&ws, o_bytes + l_bytes, stream) != cudaSuccess) {
+  if (cudaMallocAsync(&ws, bytes, stream) != cudaSuccess) {
     cudaGetLastError();
     return ATTN_ERR_ALLOC;
   }
@@ -221,50 +236,24 @@ int attn_decode_splitkv(const void* q, const void* kcache, const void* vcache, v
   return rc;
 }
 
+int attn_decode_splitkv(const void* q, const void* kcache, const void* vcache, void* o, float* lse,
+                        int B, int Hq, int Hkv, int Nk, int D, int nsplit, cudaStream_t stream) {
+  if (!o) return ATTN_ERR_NULL;
+  DecodeParams p;
+  if (int rc = decode_prepare(q, kcache, vcache, o, nullptr, lse, B, Hq, Hkv, Nk, D, nsplit, &p))
+    return rc;
+  return decode_with_scratch(p, stream);
+}
+
 int attn_decode_splitkv_states(const void* q, const void* kcache, const void* vcache,
                                float* o_state, float* lse, int B, int Hq, int Hkv, int Nk, int D,
                                int nsplit, cudaStream_t stream) {
-  if (!q || !kcache || !vcache || !o_state || !lse) return ATTN_ERR_NULL;
-  if (B < 1 || Hq < 1 || Hkv < 1 || Nk < 1 || Hq % Hkv != 0) return ATTN_ERR_SHAPE;
-  if (D != 64 && D != 128) return ATTN_ERR_SHAPE;
-  if (nsplit < 1 || nsplit > Nk) return ATTN_ERR_SHAPE;
-  if (B > 65535 || Hq > 65535) return ATTN_ERR_SHAPE;
-  if (!decode_supported(Hq / Hkv, D)) return ATTN_ERR_SHAPE;
-  if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o_state) ||
-      !aligned16(lse))
-    return ATTN_ERR_ALIGN;
-  DeviceState* st = nullptr;
-  if (int rc = device_state(&st)) return rc;
-  DecodeParams p = {};
-  p.q = q;
-  p.k = kcache;
-  p.v = vcache;
-  p.o_state = o_state;
-  p.lse = lse;
-  p.B = B;
-  p.Hq = Hq;
-  p.Hkv = Hkv;
-  p.Nk = Nk;
-  p.D = D;
-  p.nsplit = nsplit;
-  p.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(D)));
-  p.err = st->err_word;
-  p.wait_limit_ns = kWaitLimitNs;
-  const size_t o_bytes = static_cast<size_t>(B) * Hq * nsplit * D * sizeof(float);
-  const size_t l_bytes = static_cast<size_t>(B) * Hq * nsplit * sizeof(float);
-  void* ws = nullptr;
-  if (cudaMallocAsync(&ws, o_bytes + l_bytes, stream) != cudaSuccess) {
-    cudaGetLastError();
-    return ATTN_ERR_ALLOC;
-  }
-  p.ws_o = static_cast<float*>(ws);
-  p.ws_lse = reinterpret_cast<float*>(static_cast<char*>(ws) + o_bytes);
-  int rc = ATTN_OK;
-  if (launch_decode_split(p, stream) != cudaSuccess ||
-      launch_decode_combine(p, stream) != cudaSuccess)
-    rc = ATTN_ERR_LAUNCH;
-  if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == ATTN_OK) rc = ATTN_ERR_CUDA;
-  return rc;
+  if (!o_state) return ATTN_ERR_NULL;
+  DecodeParams p;
+  if (int rc =
+          decode_prepare(q, kcache, vcache, nullptr, o_state, lse, B, Hq, Hkv, Nk, D, nsplit, &p))
+    return rc;
+  return decode_with_scratch(p, stream);
 }
 
 int attn_combine_states(const float* part_o, const float* part_lse, void* o, float* lse,

@@ -40,8 +40,6 @@ struct ScratchState {
 };
 ScratchState g_state[kMaxDevices];
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 int scratch_for_current_device(float** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
@@ -69,40 +67,19 @@ extern "C" int attn_decode_splitkv_noalloc(const void* q, const void* kcache, co
                                            void* o, float* lse, int B, int Hq, int Hkv, int Nk,
                                            int D, int nsplit, cudaStream_t stream) {
   using namespace attn;
-  if (!q || !kcache || !vcache || !o || !lse) return ATTN_ERR_NULL;
-  if (B < 1 || Hq < 1 || Hkv < 1 || Nk < 1 || Hq % Hkv != 0) return ATTN_ERR_SHAPE;
-  if (D != 64 && D != 128) return ATTN_ERR_SHAPE;
-  if (nsplit < 1 || nsplit > Nk) return ATTN_ERR_SHAPE;
-  if (B > 65535 || Hq > 65535) return ATTN_ERR_SHAPE;
-  if (!decode_supported(Hq / Hkv, D)) return ATTN_ERR_SHAPE;
-  const size_t rows = static_cast<size_t>(B) * Hq * nsplit;
-  if (rows * (static_cast<size_t>(D) + 1) > kScratchFloats) return ATTN_ERR_SCRATCH;
-  if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o) ||
-      !aligned16(lse))
-    return ATTN_ERR_ALIGN;
+  if (!o) return ATTN_ERR_NULL;
+  DecodeParams p;
+  if (int rc = decode_prepare(q, kcache, vcache, o, nullptr, lse, B, Hq, Hkv, Nk, D, nsplit, &p))
+    return rc;
+  size_t o_bytes = 0;
+  if (decode_scratch_bytes(p, &o_bytes) > ATTN_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_SCRATCH;
+  if (int rc = decode_bind_device(&p)) return rc;
   float* scratch = nullptr;
   if (int rc = scratch_for_current_device(&scratch)) return rc;
-
-  DecodeParams p = {};
-  p.q = q;
-  p.k = kcache;
-  p.v = vcache;
-  p.o = o;
-  p.lse = lse;
-  p.B = B;
-  p.Hq = Hq;
-  p.Hkv = Hkv;
-  p.Nk = Nk;
-  p.D = D;
-  p.nsplit = nsplit;
-  p.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(D)));
   // Every partial state is written by the split kernel before the combine
   // kernel reads it, so the scratch needs no clearing between calls.
-  p.err = device_error_word();
-  if (!p.err) return ATTN_ERR_CUDA;
-  p.wait_limit_ns = wait_limit_ns();
   p.ws_o = scratch;
-  p.ws_lse = scratch + rows * D;
+  p.ws_lse = scratch + o_bytes / sizeof(float);
   if (launch_decode_split(p, stream) != cudaSuccess ||
       launch_decode_combine(p, stream) != cudaSuccess)
     return ATTN_ERR_LAUNCH;

@@ -23,11 +23,13 @@
 //     A operand straight from TMEM;
 //   * a TMA load warp streams K and V tiles (128 keys x D, 128-byte swizzle)
 //     through a STAGES-deep shared-memory ring;
-//   * two softmax warpgroups (thread = query row) compute row max, exp2,
-//     row sum in fp32 and publish the rescale factor; a correction warpgroup
-//     rescales O in TMEM only when some row's max rose by more than 2^8
+//   * sixteen softmax warps, eight per query tile: two warps share each
+//     32-lane TMEM quarter (16 rows each) and the two half-warps split a row's
+//     128 scores, so a thread handles 64 columns; row max (one shuffle),
+//     exp2, row sum in fp32, P packed to bf16 into TMEM.  The same warps
+//     rescale O in TMEM, only when some row's max rose by more than 2^8
 //     (otherwise the stale max stays: exact, because the final division uses
-//     the same max), then does the epilogue (O / l -> bf16 -> swizzled smem ->
+//     the same max), and run the epilogue (O / l -> bf16 -> swizzled smem ->
 //     TMA store, and LSE);
 //   * setmaxnreg moves registers from the load/MMA warps to the softmax warps.
 #include <cuda_bf16.h>

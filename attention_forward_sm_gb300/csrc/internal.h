@@ -53,6 +53,18 @@ uint64_t wait_limit_ns();
 cudaError_t launch_fwd(const FwdParams& p, cudaStream_t stream);
 size_t fwd_smem_bytes(int D);
 
+// Checks the arguments of a split-KV decode on the host (exactly one of o /
+// o_state is used; the other may be NULL) and fills every field of *p but the
+// scratch pointers and the error word.  Returns an ATTN_* status.
+int decode_prepare(const void* q, const void* kcache, const void* vcache, void* o, float* o_state,
+                   float* lse, int B, int Hq, int Hkv, int Nk, int D, int nsplit,
+                   DecodeParams* p);
+// Checks the current device (sm_103) and sets p->err to its error word.
+int decode_bind_device(DecodeParams* p);
+// Bytes of partial-state scratch a decode needs; *o_bytes = the partial
+// outputs' share (the partial lse follow them).
+size_t decode_scratch_bytes(const DecodeParams& p, size_t* o_bytes);
+
 cudaError_t launch_decode_split(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream);
 bool decode_supported(int G, int D);

@@ -333,9 +333,10 @@ def run_gpu(args):
                      "kernels": "decode_split_kernel<128,4> + decode_combine_kernel<128>"},
     }
 
-    other = None
+    other = dec_graph = None
     if not args.no_other:
         other = time_other_workloads(attn, W, dev, peaks["bf16_tflops"])
+        dec_graph = time_decode_graph(attn, W, dev, wd)
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, attn, W, wp, wd, dev, world)
@@ -362,6 +363,7 @@ def run_gpu(args):
         "clocks": clocks,
         "prefill_ms_per_call": 1e3 * pf_avg_s,
         "other_prefill_workloads": other,
+        "decode_graph": dec_graph,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -402,6 +404,54 @@ def time_other_workloads(attn, W, dev, peak_tflops, calls=3):
         out[name] = {"workload": w.label(), "ms_per_call": ms, "tflops": tf,
                      "frac_of_measured_peak": tf / peak_tflops, "frac_of_nominal_2250": tf / 2250.0,
                      "calls": n}
+        del q, k, v, o, lse
+        torch.cuda.empty_cache()
+    return out
+
+
+def time_decode_graph(attn, W, dev, wd, calls=200):
+    """Decode step as a replayed CUDA graph vs the direct call, on the decode
+    workload and on a short-context step (B1 Hq32 Hkv8 Nk4096) where fixed
+    costs weigh most.  Per call: GPU time between CUDA events over `calls`
+    back-to-back calls, and the host time to enqueue them."""
+    import torch
+    out = {}
+    small = W.custom(1, 32, 8, 1, 4096, 128, False, seed_index=950, decode=True, nsplit=8)
+    for name, w, n in (("decode", wd, 20), ("short_context", small, calls)):
+        q, k, v = W.make_inputs(w, dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
+        stream = torch.cuda.current_stream(dev)
+        sh = stream.cuda_stream
+        g = attn.DecodeGraph(q, k, v, w.nsplit)
+
+        def direct():
+            attn.attn_decode_splitkv(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.Nk, w.D, w.nsplit, sh)
+
+        def graph():
+            attn.attn_decode_graph_launch(g.handle, sh)
+
+        res = {"workload": w.label(), "calls": n}
+        for label, fn in (("direct", direct), ("graph", graph)):
+            for _ in range(5):
+                fn()
+            torch.cuda.synchronize(dev)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            t0 = time.perf_counter()
+            for _ in range(n):
+                fn()
+            host_s = time.perf_counter() - t0
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            res[f"{label}_us_per_call"] = 1e3 * a.elapsed_time(b) / n
+            res[f"{label}_host_enqueue_us_per_call"] = 1e6 * host_s / n
+        torch.cuda.synchronize(dev)
+        if not (torch.equal(o, g.o) and torch.equal(lse, g.lse)):
+            raise RuntimeError("graph replay and direct decode differ")
+        res["graph_gbs"] = w.decode_bytes() / (res["graph_us_per_call"] * 1e-6) / 1e9
+        g.close()
+        out[name] = res
         del q, k, v, o, lse
         torch.cuda.empty_cache()
     return out

@@ -180,6 +180,44 @@ int attn_decode_splitkv_noalloc(const void *q, const void *kcache, const void *v
                                 float *lse, int B, int Hq, int Hkv, int Nk, int D, int nsplit,
                                 cudaStream_t stream);
 
+/*
+ * Decode step as a replayable CUDA graph.  Source: smzdm digest of Zhihu
+ * posts, section 4: a decode step is two short kernels, so its fixed
+ * per-step costs (host launch work, the gap between the split kernel and the
+ * combine) matter; the remedy named there is a CUDA Graph around the step
+ * with programmatic dependent launch (PDL) between the kernels.
+ *
+ * attn_decode_graph_create captures attn_decode_splitkv's two kernels (the
+ * combine linked to the split by PDL) for the given buffers and sizes once,
+ * and instantiates the graph; attn_decode_graph_launch replays it on any
+ * stream of the same device: one graph launch per step, no argument checks,
+ * no allocation.  Arguments, layouts, numerics and results of a replay are
+ * those of attn_decode_splitkv on the buffers' contents at replay time.
+ *
+ *   - The handle owns its partial-state scratch (B*Hq*nsplit*(D+1)*4 bytes,
+ *     cudaMalloc'ed at create; ATTN_ERR_ALLOC if that fails) and an event.
+ *   - q, kcache, vcache, o and lse are bound by address: they must stay
+ *     allocated, at the same addresses, until the handle is destroyed;
+ *     their contents may change between replays (e.g. the next token's q).
+ *   - Replays of one handle share its scratch: order them (one stream, or
+ *     events), as for any kernel that writes the same buffer.
+ *   - create returns the same validation errors as attn_decode_splitkv, plus
+ *     ATTN_ERR_NULL for out == NULL and ATTN_ERR_CUDA if capture or
+ *     instantiation fails; nothing is left allocated on failure.  It must be
+ *     called with the target device current and no capture running on the
+ *     calling thread.
+ *   - destroy waits for the handle's last replay to finish, then frees
+ *     everything; destroy(NULL) is a no-op returning ATTN_OK.
+ */
+typedef struct attn_decode_graph attn_decode_graph;
+int attn_decode_graph_create(const void *q, const void *kcache, const void *vcache, void *o,
+                             float *lse, int B, int Hq, int Hkv, int Nk, int D, int nsplit,
+                             attn_decode_graph **out);
+/* Replays the step on `stream`; ATTN_ERR_NULL for a NULL handle,
+ * ATTN_ERR_LAUNCH if the graph launch fails. */
+int attn_decode_graph_launch(attn_decode_graph *graph, cudaStream_t stream);
+int attn_decode_graph_destroy(attn_decode_graph *graph);
+
 /* Human-readable name of an ATTN_* status code (static string). */
 const char *attn_status_string(int status);
 

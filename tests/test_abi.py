@@ -95,3 +95,20 @@ def test_states_and_combine_validation(lib):
     assert lib.attn_combine_states(A, A, A, A, 4, 0, 128, None) == -3
     assert lib.attn_combine_states(A, A, A, A, 4, 4, 96, None) == -3
     assert lib.attn_combine_states(A + 4, A, A, A, 4, 4, 128, None) == -2
+
+
+def test_decode_graph_validation(lib):
+    A = ALIGNED
+    h = ctypes.c_void_p()
+    # out == NULL
+    assert lib.attn_decode_graph_create(A, A, A, A, A, 1, 4, 2, 16, 128, 4, None) == -1
+    # NULL tensor, bad shapes, nsplit > Nk, misaligned: rejected before any CUDA call
+    assert lib.attn_decode_graph_create(A, A, A, 0, A, 1, 4, 2, 16, 128, 4, ctypes.byref(h)) == -1
+    assert lib.attn_decode_graph_create(A, A, A, A, A, 1, 4, 3, 16, 128, 4, ctypes.byref(h)) == -3
+    assert lib.attn_decode_graph_create(A, A, A, A, A, 1, 4, 2, 16, 96, 4, ctypes.byref(h)) == -3
+    assert lib.attn_decode_graph_create(A, A, A, A, A, 1, 4, 2, 16, 128, 17, ctypes.byref(h)) == -3
+    assert lib.attn_decode_graph_create(A + 8, A, A, A, A, 1, 4, 2, 16, 128, 4,
+                                        ctypes.byref(h)) == -2
+    assert h.value is None  # nothing handed out on failure
+    assert lib.attn_decode_graph_launch(None, None) == -1
+    assert lib.attn_decode_graph_destroy(None) == 0
