@@ -59,6 +59,8 @@ def _bind(lib):
     lib.oracle_attn_rows_split.argtypes = common + [i64, vp, vp, ip]
     lib.oracle_attn_rows_partials.argtypes = common + [i64, vp, vp, ip]
     lib.oracle_combine.argtypes = [vp, vp, i64, i64, i64, vp, vp]
+    lib.oracle_e4m3_to_bf16.argtypes = [vp, vp, i64]
+    lib.oracle_e4m3_to_bf16.restype = ctypes.c_int
     for f in (lib.oracle_attn_rows, lib.oracle_attn_rows_online, lib.oracle_attn_rows_split,
               lib.oracle_attn_rows_partials, lib.oracle_combine):
         f.restype = ctypes.c_int
@@ -182,3 +184,38 @@ def decode(q, kcache, vcache, B, Hq, Hkv, Nk, D, scale=None, *, nthreads=None, l
         scale = 1.0 / np.sqrt(D)
     return attn_rows(q, kcache, vcache, B, Hq, Hkv, 1, Nk, D, False, scale, None,
                      nthreads=nthreads, lib=lib)
+
+
+def e4m3_to_bf16(x, *, lib=None):
+    """FP8 E4M3 codes (a uint8 / float8_e4m3fn tensor or uint8 array) -> the
+    same values as a bf16 tensor (exact: every E4M3 value is a bf16 value).
+    Raises on a NaN code."""
+    import torch
+    lib = lib or load()
+    if isinstance(x, torch.Tensor):
+        a = np.ascontiguousarray(x.detach().cpu().contiguous().view(torch.uint8).numpy())
+        shape = tuple(x.shape)
+    else:
+        a = np.ascontiguousarray(np.asarray(x, dtype=np.uint8))
+        shape = a.shape
+    out = np.zeros(a.size, dtype=np.uint16)
+    if lib.oracle_e4m3_to_bf16(a.ctypes.data, out.ctypes.data, a.size) != 0:
+        raise ValueError("NaN code in FP8 input")
+    return torch.from_numpy(out.view(np.int16)).view(torch.bfloat16).reshape(shape)
+
+
+def attn_rows_fp8(q8, k8, v8, B, Hq, Hkv, Nq, Nk, D, causal, scale, q_scale, k_scale, v_scale,
+                  rows=None, *, nthreads=None, lib=None):
+    """Attention on FP8 E4M3 inputs with per-tensor dequantisation scales:
+    the real operands are q_scale*Q8, k_scale*K8, v_scale*V8 (Q8, K8, V8 the
+    decoded codes; V8 as [B, Hkv, Nk, D]).  Scores are
+    scale * <q_scale Q8_i, k_scale K8_j> = (scale*q_scale*k_scale) <Q8_i, K8_j>,
+    and O is linear in V, so this is the fp64 definition above on the decoded
+    codes with the score scale folded and O multiplied by v_scale (LSE does
+    not depend on V).  Returns O [rows, D], LSE [rows] in fp64."""
+    lib = lib or load()
+    qb, kb, vb = (e4m3_to_bf16(t, lib=lib) for t in (q8, k8, v8))
+    o, lse = attn_rows(qb, kb, vb, B, Hq, Hkv, Nq, Nk, D, causal,
+                       float(scale) * float(q_scale) * float(k_scale), rows,
+                       nthreads=nthreads, lib=lib)
+    return o * float(v_scale), lse

@@ -316,6 +316,26 @@ int oracle_attn_rows_partials(const uint16_t *q, const uint16_t *k, const uint16
   return run(p, nthreads);
 }
 
+/* FP8 E4M3 ("fn" flavour of the OCP 8-bit floating-point format, the
+ * low-precision tensor-core input the FlashAttention-3 page names):
+ * 1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits; exponent field 0
+ * holds subnormals m/8 * 2^-6; no infinities; S.1111.111 is NaN.  Every such
+ * value has at most 4 significant bits and an exponent in [-9, 8], so it is
+ * exactly a bf16 value: out[i] gets those bf16 bits.  Returns -3 (and stops)
+ * at a NaN code, 0 otherwise. */
+int oracle_e4m3_to_bf16(const uint8_t *in, uint16_t *out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) {
+    const unsigned sign = in[i] >> 7, e = (in[i] >> 3) & 15u, m = in[i] & 7u;
+    if (e == 15u && m == 7u) return -3;
+    const double mag = (e == 0u) ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, (int)e - 7);
+    const float f = (float)(sign ? -mag : mag);
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    out[i] = (uint16_t)(u >> 16);
+  }
+  return 0;
+}
+
 /* Log-sum-exp combine of partial states: part_o [nrows, nsplit, D],
  * part_lse [nrows, nsplit] -> out_o [nrows, D], out_lse [nrows]. */
 int oracle_combine(const double *part_o, const double *part_lse, int64_t nrows, int64_t nsplit,

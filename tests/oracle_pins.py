@@ -373,11 +373,83 @@ def pin_decode_matches_prefill_last_row(lib):
     np.testing.assert_array_equal(ld, lp)
 
 
+# --------------------------------------------------------------------------- FP8 inputs
+
+
+# Code -> value facts of the E4M3 format (OCP 8-bit floating point): zero,
+# the smallest subnormal 2^-9, the largest subnormal 7 * 2^-9, the smallest
+# normal 2^-6, one, 1 + 1/8, two, the largest finite value 448, and the
+# sign bit.
+E4M3_FACTS = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x38: 1.0,
+              0x39: 1.125, 0x40: 2.0, 0x7E: 448.0, 0xB8: -1.0, 0xFE: -448.0, 0x81: -(2.0 ** -9)}
+
+
+def pin_e4m3_format_facts(lib):
+    """Values the format fixes, and NaN codes rejected."""
+    codes = torch.tensor(sorted(E4M3_FACTS), dtype=torch.uint8)
+    got = oracle.e4m3_to_bf16(codes, lib=lib).double().tolist()
+    assert got == [E4M3_FACTS[c] for c in sorted(E4M3_FACTS)], got
+    for nan_code in (0x7F, 0xFF):
+        try:
+            oracle.e4m3_to_bf16(torch.tensor([nan_code], dtype=torch.uint8), lib=lib)
+        except ValueError:
+            continue
+        raise AssertionError(f"NaN code {nan_code:#x} accepted")
+
+
+def pin_e4m3_matches_torch_and_is_monotone(lib):
+    """All 254 finite codes equal torch's own float8_e4m3fn decoding (an
+    independent library routine); positive codes increase strictly and the
+    sign bit negates."""
+    codes = torch.tensor([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=torch.uint8)
+    got = oracle.e4m3_to_bf16(codes, lib=lib).double()
+    ref = codes.view(torch.float8_e4m3fn).double()
+    assert torch.equal(got, ref)
+    pos = got[:127]
+    assert bool((pos[1:] > pos[:-1]).all())
+    assert torch.equal(got[127:], -pos)
+
+
+def rand_e4m3(shape, seed, sigma=1.0):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(shape, generator=g) * sigma).clamp(-448, 448).to(torch.float8_e4m3fn)
+
+
+def pin_fp8_brute_force_with_scales(lib):
+    """FP8 attention with dequantisation scales against a pure-Python fp64
+    computation on torch-decoded codes (q_scale*Q, k_scale*K, v_scale*V)."""
+    Hq, Hkv, Nq, Nk, D = 2, 1, 6, 9, 8
+    q8, k8, v8 = (rand_e4m3((1, h, n, D), 900 + i)
+                  for i, (h, n) in enumerate(((Hq, Nq), (Hkv, Nk), (Hkv, Nk))))
+    scale, qs, ks, vs = 0.3, 1.5, 0.75, 2.5
+    Q = (q8.double() * qs).tolist()
+    K = (k8.double() * ks).tolist()
+    V = (v8.double() * vs).tolist()
+    for causal in (False, True):
+        want_o, want_l = [], []
+        for h in range(Hq):
+            for i in range(Nq):
+                keys = [j for j in range(Nk) if (not causal or j <= i)]
+                s_ = [scale * math.fsum(Q[0][h][i][d] * K[0][0][j][d] for d in range(D))
+                      for j in keys]
+                m = max(s_)
+                e = [math.exp(x - m) for x in s_]
+                z = math.fsum(e)
+                want_l.append(m + math.log(z))
+                want_o.append([math.fsum(e[t] / z * V[0][0][j][d] for t, j in enumerate(keys))
+                               for d in range(D)])
+        o, l = oracle.attn_rows_fp8(q8, k8, v8, 1, Hq, Hkv, Nq, Nk, D, causal, scale, qs, ks, vs,
+                                    lib=lib)
+        np.testing.assert_allclose(o, np.array(want_o), rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(l, np.array(want_l), rtol=1e-13, atol=1e-13)
+
+
 ALL_PINS = [
     pin_rows_are_distributions, pin_constant_values, pin_single_key, pin_causal_row0,
     pin_uniform_attention, pin_two_keys_closed_form, pin_golden_hand_worked, pin_key_permutation,
     pin_value_linearity, pin_shift_invariance, pin_online_equals_two_pass,
     pin_split_equals_unsplit, pin_naive_partial_sum_is_wrong, pin_gqa_is_repeated_mha,
     pin_row_subset_consistency, pin_textbook_torch_float64, pin_brute_force_fsum,
-    pin_decode_matches_prefill_last_row,
+    pin_decode_matches_prefill_last_row, pin_e4m3_format_facts,
+    pin_e4m3_matches_torch_and_is_monotone, pin_fp8_brute_force_with_scales,
 ]

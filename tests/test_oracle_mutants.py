@@ -45,6 +45,11 @@ MUTANTS = {
     "combine_weight_unnormalised": ("const double w = exp(plse[c] - L);",
                                     "const double w = exp(plse[c] - mx);"),
     "combine_lse_is_max": ("const double L = mx + log(sum);", "const double L = mx;"),
+    "e4m3_bias_6": ("ldexp(1.0 + (double)m / 8.0, (int)e - 7)", "ldexp(1.0 + (double)m / 8.0, (int)e - 6)"),
+    "e4m3_subnormal_exponent": ("ldexp((double)m / 8.0, -6)", "ldexp((double)m / 8.0, -7)"),
+    "e4m3_mantissa_sixteenths": ("ldexp(1.0 + (double)m / 8.0,", "ldexp(1.0 + (double)m / 16.0,"),
+    "e4m3_sign_ignored": ("const float f = (float)(sign ? -mag : mag);", "const float f = (float)mag;"),
+    "e4m3_nan_accepted": ("if (e == 15u && m == 7u) return -3;", ""),
 }
 
 
