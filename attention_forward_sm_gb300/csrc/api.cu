@@ -89,6 +89,23 @@ int encode_3d(CUtensorMap* map, const void* base, int D, int N, long long BH) {
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_TMA;
 }
 
+// 3-D view [BH, rows, inner] of a contiguous e4m3 tensor (bytes), box
+// {128, 128, 1}, 128-byte swizzle.  `inner` * 1 byte must be a multiple of 16.
+int encode_3d_e4m3(CUtensorMap* map, const void* base, int inner, int rows, long long BH) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn;
+  if (int rc = encode_fn(&fn)) return rc;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner),
+                           static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(inner)};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_TMA;
+}
+
 // One CTA waits, through the same bounded wait the pipelines use, on an
 // mbarrier that nothing ever arrives at; the wait gives up after `limit_ns`
 // and records `kErrSelfTest` in the device error word.
@@ -210,6 +227,46 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.D = D;
   p.causal = causal ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.o_scale = 1.f;
+  p.err = st->err_word;
+  p.wait_limit_ns = kWaitLimitNs;
+  if (launch_fwd(p, stream) != cudaSuccess) return ATTN_ERR_LAUNCH;
+  return ATTN_OK;
+}
+
+int attn_fwd_fp8(const void* q, const void* k, const void* vt, void* o, float* lse, int B, int Hq,
+                 int Hkv, int Nq, int Nk, int D, int causal, float scale, float q_scale,
+                 float k_scale, float v_scale, cudaStream_t stream) {
+  if (!q || !k || !vt || !o || !lse) return ATTN_ERR_NULL;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nk < 1 || Hq % Hkv != 0) return ATTN_ERR_SHAPE;
+  if (D != 128 || Nk % 16 != 0) return ATTN_ERR_SHAPE;
+  for (float x : {scale, q_scale, k_scale, v_scale})
+    if (!isfinite(x) || x < 0.f) return ATTN_ERR_SHAPE;
+  const float s_qk = scale * q_scale * k_scale;
+  if (!isfinite(s_qk)) return ATTN_ERR_SHAPE;
+  const long long nqb = (Nq + 255) / 256;
+  if (static_cast<long long>(B) * Hq * nqb >= (1ll << 31)) return ATTN_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(vt) || !aligned16(o) || !aligned16(lse))
+    return ATTN_ERR_ALIGN;
+  DeviceState* st = nullptr;
+  if (int rc = device_state(&st)) return rc;
+
+  FwdParams p = {};
+  if (int rc = encode_3d_e4m3(&p.tmap_q, q, D, Nq, static_cast<long long>(B) * Hq)) return rc;
+  if (int rc = encode_3d_e4m3(&p.tmap_k, k, D, Nk, static_cast<long long>(B) * Hkv)) return rc;
+  if (int rc = encode_3d_e4m3(&p.tmap_v, vt, Nk, D, static_cast<long long>(B) * Hkv)) return rc;
+  if (int rc = encode_3d(&p.tmap_o, o, D, Nq, static_cast<long long>(B) * Hq)) return rc;
+  p.lse = lse;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.D = D;
+  p.causal = causal ? 1 : 0;
+  p.fp8 = 1;
+  p.scale_log2 = s_qk * 1.4426950408889634f;
+  p.o_scale = v_scale;
   p.err = st->err_word;
   p.wait_limit_ns = kWaitLimitNs;
   if (launch_fwd(p, stream) != cudaSuccess) return ATTN_ERR_LAUNCH;

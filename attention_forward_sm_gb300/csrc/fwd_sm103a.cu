@@ -50,21 +50,37 @@ constexpr int kWarpMma = 17;
 // 4 softmax warpgroups + 1 warpgroup for load / MMA / idle warps.
 constexpr uint32_t kRegSoftmax = 112, kRegOther = 32;
 static_assert(4 * 128 * kRegSoftmax + 128 * kRegOther <= 640 * 96, "register split");
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max rises > 2^8
 
-template <int D>
+template <int D, bool kFp8 = false>
 struct Cfg {
-  static constexpr int kTileBytes = kBM * D * 2;      // one 128 x D bf16 tile
-  static constexpr int kChunks = D / 64;              // 64-column swizzle chunks per tile
-  static constexpr int kStages = (D == 128) ? 4 : 8;  // K/V ring depth
+  static constexpr int kElemBytes = kFp8 ? 1 : 2;
+  static constexpr int kTileBytes = kBM * D * kElemBytes;  // a 128 x D tile (Q, K; V or V^T)
+  static constexpr int kAtomElems = 128 / kElemBytes;      // elements per 128-byte swizzle row
+  static constexpr int kChunks = D * kElemBytes / 128;     // 128-byte swizzle chunks per tile row
+  static constexpr int kStages = (D == 128) ? 4 : 8;       // K/V ring depth
+  static constexpr int kOutTileBytes = kBM * D * 2;        // a bf16 O tile
+  static constexpr int kOutChunks = D / 64;
   static constexpr int kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
   static constexpr int kTmemCols = 512;
-  // shared memory map (offsets from a 1024-byte aligned base)
+  // P = 2^(s - m + kPBias) and the running max moves when it rises by more
+  // than kRescale (log2 units).  bf16 P has fp32's range: any bias works, a
+  // wide threshold saves O rescales.  E4M3 P saturates at 448 < 2^9, so
+  // p <= 2^(kPBias + kRescale) must stay <= 2^8; the bias lifts small
+  // weights out of the subnormal range (normal E4M3 starts at 2^-6).
+  static constexpr float kPBias = kFp8 ? 6.f : 0.f;
+  static constexpr float kRescale = kFp8 ? 2.f : 8.f;
+  // shared memory map (offsets from a 1024-byte aligned base).  O is staged
+  // for the TMA store in the tile's Q buffer when that holds a bf16 tile,
+  // else in a buffer of its own.
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = 2 * kTileBytes;
-  static constexpr int kOffMisc = kOffKV + kStages * kTileBytes;
+  static constexpr int kOffStage = kFp8 ? kOffKV + kStages * kTileBytes : kOffQ;
+  static constexpr int kOffMisc =
+      kFp8 ? kOffStage + 2 * kOutTileBytes : kOffKV + kStages * kTileBytes;
   static constexpr int kMiscBytes = 4096;
   static constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;  // + alignment slack
+  static_assert(!kFp8 || D == kBN, "the FP8 V^T tile is D x 128 keys: D must be 128");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 
 struct Misc {
@@ -105,79 +121,46 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return;
 }
 
-// 64 consecutive TMEM columns of this thread's lane from registers, one wait.
-#define ATTN_W8(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), "r"(r[i + 4]), \
-    "r"(r[i + 5]), "r"(r[i + 6]), "r"(r[i + 7])
-__device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&r)[64]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%64], {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, "
-      "%10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, "
-      "%27, %28, %29, %30, %31};\n\t"
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%65], {%32, %33, %34, %35, %36, %37, %38, %39, "
-      "%40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, "
-      "%57, %58, %59, %60, %61, %62, %63};\n\t"
-      "tcgen05.wait::st.sync.aligned;" ::ATTN_W8(0),
-      ATTN_W8(8), ATTN_W8(16), ATTN_W8(24), ATTN_W8(32), ATTN_W8(40), ATTN_W8(48), ATTN_W8(56),
-      "r"(taddr), "r"(taddr + 32)
-      : "memory");
-}
-#undef ATTN_W8
-
-// 128 consecutive TMEM columns of this thread's lane, one wait.
-#define ATTN_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), \
-    "=r"(r[i + 4]), "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
-__device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
-      "%28, %29, %30, %31}, [%128];\n\t"
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32, %33, %34, %35, %36, %37, %38, %39, %40, "
-      "%41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, "
-      "%58, %59, %60, %61, %62, %63}, [%129];\n\t"
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%64, %65, %66, %67, %68, %69, %70, %71, %72, "
-      "%73, %74, %75, %76, %77, %78, %79, %80, %81, %82, %83, %84, %85, %86, %87, %88, %89, "
-      "%90, %91, %92, %93, %94, %95}, [%130];\n\t"
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%96, %97, %98, %99, %100, %101, %102, %103, "
-      "%104, %105, %106, %107, %108, %109, %110, %111, %112, %113, %114, %115, %116, %117, "
-      "%118, %119, %120, %121, %122, %123, %124, %125, %126, %127}, [%131];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : ATTN_R8(0), ATTN_R8(8), ATTN_R8(16), ATTN_R8(24), ATTN_R8(32), ATTN_R8(40), ATTN_R8(48),
-        ATTN_R8(56), ATTN_R8(64), ATTN_R8(72), ATTN_R8(80), ATTN_R8(88), ATTN_R8(96),
-        ATTN_R8(104), ATTN_R8(112), ATTN_R8(120)
-      : "r"(taddr), "r"(taddr + 32), "r"(taddr + 64), "r"(taddr + 96)
-      : "memory");
-}
-#undef ATTN_R8
-
-// S = Q K^T over the head dimension: D/16 k-steps of 16 columns; inside a
-// 128-byte swizzle chunk a k-step advances the start address by 32 bytes,
-// the next 64-column chunk starts 128 rows * 128 bytes further.
-template <int KK, int NK>
+// S = Q K^T over the head dimension, one MMA per 32 bytes of a row (16 bf16
+// or 32 e4m3 columns); inside a 128-byte swizzle chunk a k-step advances the
+// start address by 32 bytes, the next chunk starts 128 rows * 128 bytes
+// further.
+template <bool kFp8, int KK, int NK>
 __device__ __forceinline__ void issue_s_rec(uint32_t d, uint64_t a0, uint64_t b0, uint32_t idesc) {
   if constexpr (KK < NK) {
     constexpr uint32_t off = ((KK >> 2) * (kBM * 128) + (KK & 3) * 32) >> 4;
-    mma_ss_off<off, off>(d, a0, b0, idesc, KK > 0 ? 1u : 0u);
-    issue_s_rec<KK + 1, NK>(d, a0, b0, idesc);
+    if constexpr (kFp8)
+      mma_ss_off_f8<off, off>(d, a0, b0, idesc, KK > 0 ? 1u : 0u);
+    else
+      mma_ss_off<off, off>(d, a0, b0, idesc, KK > 0 ? 1u : 0u);
+    issue_s_rec<kFp8, KK + 1, NK>(d, a0, b0, idesc);
   }
 }
-template <int D>
+template <int D, bool kFp8>
 __device__ __forceinline__ void issue_s_steps(uint32_t d, uint64_t a0, uint64_t b0,
                                               uint32_t idesc) {
-  issue_s_rec<0, D / 16>(d, a0, b0, idesc);
+  issue_s_rec<kFp8, 0, D * (kFp8 ? 1 : 2) / 32>(d, a0, b0, idesc);
 }
-// O += P V over the keys: 8 k-steps of 16 keys; P packs 2 keys per TMEM
-// column (8 columns per step), V advances 16 rows * 128 bytes per step.
-template <int KK>
+// O += P V over the 128 keys of a tile, one MMA per 8 TMEM columns of P
+// (16 bf16 or 32 e4m3 keys).  bf16: V is MN-major, a step advances 16 rows
+// * 128 bytes.  e4m3: V^T (D rows of 128 keys) is K-major, a step advances
+// 32 bytes inside the 128-byte row.
+template <bool kFp8, int KK>
 __device__ __forceinline__ void issue_pv_rec(uint32_t d, uint32_t a, uint64_t b0, uint32_t idesc,
                                              uint32_t acc) {
-  if constexpr (KK < kBN / 16) {
-    mma_ts_off<((KK * 16 * 128) >> 4)>(d, a + KK * 8, b0, idesc, (acc | KK) ? 1u : 0u);
-    issue_pv_rec<KK + 1>(d, a, b0, idesc, acc);
+  constexpr int kSteps = kFp8 ? kBN / 32 : kBN / 16;
+  if constexpr (KK < kSteps) {
+    if constexpr (kFp8)
+      mma_ts_off_f8<((KK * 32) >> 4)>(d, a + KK * 8, b0, idesc, (acc | KK) ? 1u : 0u);
+    else
+      mma_ts_off<((KK * 16 * 128) >> 4)>(d, a + KK * 8, b0, idesc, (acc | KK) ? 1u : 0u);
+    issue_pv_rec<kFp8, KK + 1>(d, a, b0, idesc, acc);
   }
 }
+template <bool kFp8>
 __device__ __forceinline__ void issue_pv_steps(uint32_t d, uint32_t a, uint64_t b0, uint32_t idesc,
                                                uint32_t acc) {
-  issue_pv_rec<0>(d, a, b0, idesc, acc);
+  issue_pv_rec<kFp8, 0>(d, a, b0, idesc, acc);
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
@@ -187,10 +170,10 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
-template <int D>
+template <int D, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ FwdParams p) {
-  using C = Cfg<D>;
+  using C = Cfg<D, kFp8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -303,27 +286,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       // running max in log2 units (scale >= 0, so max commutes with scaling)
       const float m_tile = (mx == -CUDART_INF_F) ? -CUDART_INF_F : mx * p.scale_log2;
       float alpha = 1.f;
-      if (m_tile > m + kRescaleThreshold || m == -CUDART_INF_F) {
+      if (m_tile > m + C::kRescale || m == -CUDART_INF_F) {
         alpha = ex2_approx(m - m_tile);  // 0 on the first tile
         m = m_tile;
       }
       if (tracer) ATTN_TRACE_EV(2, t, j);
-      // p = 2^(s*scale*log2e - m), masked entries exactly 0
-      const float neg_m = -m;
+      // p = 2^(s*scale*log2e - m + bias), masked entries exactly 0; packed
+      // to bf16 pairs (32 words) or e4m3 quads (16 words), low key first
+      const float neg_m = C::kPBias - m;
       float rsum;
-      uint32_t pk[32];
+      uint32_t pk[kFp8 ? 16 : 32];
+      auto pack4 = [&](int i, float p0, float p1, float p2, float p3) {
+        if constexpr (kFp8) {
+          pk[i / 4] = pack_e4m3x4(p0, p1, p2, p3);
+        } else {
+          pk[i / 2] = pack_bf16x2(p0, p1);
+          pk[i / 2 + 1] = pack_bf16x2(p2, p3);
+        }
+      };
       if (need_mask) {
         float r0 = 0.f, r1 = 0.f;
 #pragma unroll
-        for (int i = 0; i < 64; i += 2) {
-          const float p0 =
-              (s[i] == -CUDART_INF_F) ? 0.f : ex2_approx(fmaf(s[i], p.scale_log2, neg_m));
-          const float p1 = (s[i + 1] == -CUDART_INF_F)
-                               ? 0.f
-                               : ex2_approx(fmaf(s[i + 1], p.scale_log2, neg_m));
-          r0 += p0;
-          r1 += p1;
-          pk[i / 2] = pack_bf16x2(p0, p1);
+        for (int i = 0; i < 64; i += 4) {
+          float pp[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            pp[u] = (s[i + u] == -CUDART_INF_F) ? 0.f
+                                                : ex2_approx(fmaf(s[i + u], p.scale_log2, neg_m));
+          r0 += pp[0] + pp[2];
+          r1 += pp[1] + pp[3];
+          pack4(i, pp[0], pp[1], pp[2], pp[3]);
         }
         rsum = r0 + r1;
       } else {
@@ -340,8 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
           acc0 = add_f32x2(acc0, f32x2(p0, p1));
           acc1 = add_f32x2(acc1, f32x2(p2, p3));
-          pk[i / 2] = pack_bf16x2(p0, p1);
-          pk[i / 2 + 1] = pack_bf16x2(p2, p3);
+          pack4(i, p0, p1, p2, p3);
         }
         float u0, u1;
         unpack_f32x2(add_f32x2(acc0, acc1), u0, u1);
@@ -364,8 +355,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st_wait();
       }
-      // P (bf16 pairs) over the first 64 columns of S: this half's 32 columns
-      tmem_st_pair32<32>(s_addr, pk);
+      // P over the first 64 (bf16) or 32 (e4m3) columns of S: this half's
+      // 32 or 16 columns
+      if constexpr (kFp8)
+        tmem_st_pair16<16>(s_addr, pk);
+      else
+        tmem_st_pair32<32>(s_addr, pk);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -378,10 +373,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float l_row = l + __shfl_xor_sync(0xFFFFFFFFu, l, 16);
     const bool good =
         ok && warp_all(mbar_wait(&ms.o_done[t], 0, abort_flag, p.err, kErrWaitCorr, lim));
-    uint8_t* stage = smem + C::kOffQ + t * C::kTileBytes;
+    uint8_t* stage = smem + C::kOffStage + t * C::kOutTileBytes;
     if (good) {
       tc_fence_after();
-      const float inv = 1.f / l_row;
+      const float inv = p.o_scale / l_row;
       const uint32_t stage_row = smem_u32(stage) + r * 128;
 #pragma unroll
       for (int k = 0; k < D / 64; ++k) {
@@ -403,14 +398,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (c == 0 && row < p.Nq)
         p.lse[static_cast<size_t>(bh) * p.Nq + row] =
-            (m + __log2f(l_row)) * 0.69314718055994530942f;
+            (m - C::kPBias + __log2f(l_row)) * 0.69314718055994530942f;
     }
     fence_proxy_async_smem();
     named_bar_sync(1 + t, 256);
     if ((warp & 7) == 0 && lane == 0) {
       if (!*abort_flag && q_base + t * kBM < p.Nq) {
 #pragma unroll
-        for (int ch = 0; ch < C::kChunks; ++ch)
+        for (int ch = 0; ch < C::kOutChunks; ++ch)
           tma_store_3d(&p.tmap_o, stage + ch * (kBM * 128), ch * 64, q_base + t * kBM, bh);
         tma_store_commit();
       }
@@ -428,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = 0; t < 2; ++t)
         for (int ch = 0; ch < C::kChunks; ++ch)
           tma_load_3d(smem + C::kOffQ + t * C::kTileBytes + ch * (kBM * 128), &p.tmap_q,
-                      &ms.q_full, ch * 64, q_base + t * kBM, bh, pol_q);
+                      &ms.q_full, ch * C::kAtomElems, q_base + t * kBM, bh, pol_q);
       int issued = 0;
       for (int it = 0; it < 2 * n_kv; ++it) {
         const int s = it % C::kStages;
@@ -436,11 +431,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&ms.kv_empty[s], ph ^ 1u, abort_flag, p.err, kErrWaitLoad, lim)) break;
         ATTN_TRACE_EV(7, it & 1, it >> 1);
         mbar_arrive_expect_tx(&ms.kv_full[s], C::kTileBytes);
-        const CUtensorMap* map = (it & 1) ? &p.tmap_v : &p.tmap_k;
         uint8_t* dst = smem + C::kOffKV + s * C::kTileBytes;
-        for (int ch = 0; ch < C::kChunks; ++ch)
-          tma_load_3d(dst + ch * (kBM * 128), map, &ms.kv_full[s], ch * 64, (it >> 1) * kBN, bhkv,
-                      pol_kv);
+        if (kFp8 && (it & 1)) {
+          // V^T [D rows, keys]: rows 0..D-1, keys of tile it/2
+          tma_load_3d(dst, &p.tmap_v, &ms.kv_full[s], (it >> 1) * kBN, 0, bhkv, pol_kv);
+        } else {
+          const CUtensorMap* map = (it & 1) ? &p.tmap_v : &p.tmap_k;
+          for (int ch = 0; ch < C::kChunks; ++ch)
+            tma_load_3d(dst + ch * (kBM * 128), map, &ms.kv_full[s], ch * C::kAtomElems,
+                        (it >> 1) * kBN, bhkv, pol_kv);
+        }
         issued = it + 1;
       }
       if (*abort_flag) {
@@ -457,28 +457,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     // =====================================================================
     reg_dealloc<kRegOther>();
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, kBN, false);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
+      constexpr uint32_t idesc_s =
+          kFp8 ? idesc_e4m3_f32(128, kBN) : idesc_bf16_f32(128, kBN, false);
+      constexpr uint32_t idesc_pv = kFp8 ? idesc_e4m3_f32(128, D) : idesc_bf16_f32(128, D, true);
       constexpr uint32_t kTileDesc = C::kTileBytes >> 4;  // one tile in descriptor units
       // Descriptors are built once; every k-step only adds a constant to the
       // start-address field, so issuing an MMA costs a couple of instructions.
       const uint64_t desc_q = sdesc_sw128(smem_u32(smem + C::kOffQ), 16, 1024);
       const uint64_t desc_k = sdesc_sw128(smem_u32(smem + C::kOffKV), 16, 1024);
-      const uint64_t desc_v = sdesc_sw128(smem_u32(smem + C::kOffKV), kBM * 128, 1024);
+      // V: bf16 MN-major (64-column chunks kBM * 128 bytes apart); e4m3 V^T K-major
+      const uint64_t desc_v =
+          sdesc_sw128(smem_u32(smem + C::kOffKV), kFp8 ? 16 : kBM * 128, 1024);
       bool ok = mbar_wait(&ms.q_full, 0, abort_flag, p.err, kErrWaitMma, lim);
       // S_t = Q_t K^T from the K tile in ring slot `slot`
       auto issue_s = [&](int t, uint32_t slot) {
         const uint64_t a0 = desc_q + static_cast<uint32_t>(t) * kTileDesc;
         const uint64_t b0 = desc_k + slot * kTileDesc;
         const uint32_t d = tmem + (t ? C::kColS1 : C::kColS0);
-        issue_s_steps<D>(d, a0, b0, idesc_s);
+        issue_s_steps<D, kFp8>(d, a0, b0, idesc_s);
       };
       // O_t (+)= P_t V from the V tile in ring slot `slot`; P_t is in TMEM over S_t
       auto issue_pv = [&](int t, uint32_t slot, uint32_t acc) {
         const uint64_t b0 = desc_v + slot * kTileDesc;
         const uint32_t a = tmem + (t ? C::kColS1 : C::kColS0);
         const uint32_t d = tmem + (t ? C::kColO1 : C::kColO0);
-        issue_pv_steps(d, a, b0, idesc_pv, acc);
+        issue_pv_steps<kFp8>(d, a, b0, idesc_pv, acc);
       };
       // wait for P_t of KV tile jv (O_t is already rescaled when it arrives)
       auto wait_p = [&](int t, int jv) -> bool {
@@ -543,9 +546,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool kFp8>
 cudaError_t launch_d(const FwdParams& p, cudaStream_t stream) {
-  using C = Cfg<D>;
+  using C = Cfg<D, kFp8>;
   // the shared-memory opt-in is a per-device property of the function
   static bool attr_done[64] = {};
   int dev = 0;
@@ -553,26 +556,28 @@ cudaError_t launch_d(const FwdParams& p, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_done[dev]) {
-    e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(attn_fwd_kernel<D, kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
   const long long nqb = (p.Nq + 2 * kBM - 1) / (2 * kBM);
   const long long grid = nqb * p.B * p.Hq;
-  attn_fwd_kernel<D><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(p);
+  attn_fwd_kernel<D, kFp8><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t fwd_smem_bytes(int D) {
+size_t fwd_smem_bytes(int D, bool fp8) {
+  if (fp8) return Cfg<128, true>::kSmemBytes;
   return D == 128 ? Cfg<128>::kSmemBytes : Cfg<64>::kSmemBytes;
 }
 
 cudaError_t launch_fwd(const FwdParams& p, cudaStream_t stream) {
-  if (p.D == 128) return launch_d<128>(p, stream);
-  if (p.D == 64) return launch_d<64>(p, stream);
+  if (p.fp8) return p.D == 128 ? launch_d<128, true>(p, stream) : cudaErrorInvalidValue;
+  if (p.D == 128) return launch_d<128, false>(p, stream);
+  if (p.D == 64) return launch_d<64, false>(p, stream);
   return cudaErrorInvalidValue;
 }
 

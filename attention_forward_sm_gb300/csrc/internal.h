@@ -17,14 +17,18 @@ enum : unsigned int {
   kErrSelfTest = 1u << 4,     // the wait self-test ran out, as intended
 };
 
-// Forward (prefill) launch parameters.  Tensor maps are 3-D views
-// [B*H, N, D] of the bf16 tensors, box {64, 128, 1}, 128-byte swizzle.
+// Forward (prefill) launch parameters.  Tensor maps are 3-D views with a
+// 128-byte swizzle: bf16 [B*H, N, D] with box {64, 128, 1}; for FP8, e4m3
+// Q and K [B*H, N, D] with box {128, 128, 1} and V^T [B*Hkv, D, Nk] with box
+// {128 keys, 128 rows, 1}; O is always bf16.
 struct FwdParams {
   CUtensorMap tmap_q, tmap_k, tmap_v, tmap_o;
   float* lse;          // [B, Hq, Nq] fp32
   int B, Hq, Hkv, Nq, Nk, D;
   int causal;
-  float scale_log2;    // scale * log2(e)
+  int fp8;             // e4m3 Q, K, V^T
+  float scale_log2;    // scale * log2(e) (FP8: times q_scale * k_scale)
+  float o_scale;       // O multiplier (FP8: v_scale; bf16: 1)
   unsigned int* err;   // device error word
   uint64_t wait_limit_ns;
 };
@@ -51,7 +55,7 @@ unsigned int* device_error_word();
 uint64_t wait_limit_ns();
 
 cudaError_t launch_fwd(const FwdParams& p, cudaStream_t stream);
-size_t fwd_smem_bytes(int D);
+size_t fwd_smem_bytes(int D, bool fp8);
 
 // Checks the arguments of a split-KV decode on the host (exactly one of o /
 // o_state is used; the other may be NULL) and fills every field of *p but the

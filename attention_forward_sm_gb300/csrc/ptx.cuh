@@ -170,6 +170,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, bo
          ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
+// Instruction descriptor, kind::f8f6f4: e4m3 x e4m3 -> fp32, dense, both
+// operands K-major: [4,6) D format (1 = f32), A and B formats 0 (= E4M3).
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t M, uint32_t N) {
+  return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand.
 //   [0,14) start >> 4, [16,30) leading byte offset >> 4, [32,46) stride byte
 //   offset >> 4, [46,49) = 0b001, [49,52) base offset (0: tiles are 1024-B
@@ -229,6 +235,30 @@ __device__ __forceinline__ void mma_ts_off(uint32_t d_tmem, uint32_t a_tmem, uin
       "add.s64 db, %2, %5;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "n"(kOffB)
+      : "memory");
+}
+// kind::f8f6f4 (e4m3 operands, K = 32 per instruction) versions of the two above.
+template <uint32_t kOffA, uint32_t kOffB>
+__device__ __forceinline__ void mma_ss_off_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "add.s64 da, %1, %5;\n\t"
+      "add.s64 db, %2, %6;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "n"(kOffA), "n"(kOffB)
+      : "memory");
+}
+template <uint32_t kOffB>
+__device__ __forceinline__ void mma_ts_off_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+      "add.s64 db, %2, %5;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], db, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "n"(kOffB)
       : "memory");
 }
@@ -328,6 +358,17 @@ __device__ __forceinline__ void tmem_st_pair32(uint32_t taddr, const uint32_t (&
 }
 #undef ATTN_W8
 
+template <uint32_t kHalf>
+__device__ __forceinline__ void tmem_st_pair16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x32bx2.x16.b32 [%0], %17, {%1, %2, %3, %4, %5, %6, %7, %8, %9, "
+      "%10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "n"(kHalf)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -371,6 +412,18 @@ __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Four floats -> four e4m3 codes (round to nearest even, saturating to the
+// largest finite value), p0 in the lowest byte.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float p0, float p1, float p2, float p3) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r)
+      : "f"(p0), "f"(p1), "f"(p2), "f"(p3));
   return r;
 }
 

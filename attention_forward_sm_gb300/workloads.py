@@ -111,6 +111,34 @@ def make_inputs(w: Workload, device="cpu"):
     return q, k, v
 
 
+# Per-tensor dequantisation scales of the FP8 inputs (arbitrary, not 1, so
+# that a dropped or swapped scale shows).
+FP8_SCALES = {"q": 0.5, "k": 1.25, "v": 0.75}
+
+
+def make_inputs_fp8(w: Workload, device="cpu"):
+    """(q8, k8, v8, vt8) E4M3 code tensors (torch.float8_e4m3fn) for a prefill
+    workload ``w``: ``randn * sigma`` in fp32, clamped to the largest finite
+    E4M3 value 448, rounded to E4M3 by torch's conversion; Q, K, V drawn in
+    that order from the workload's seed + 50000.  vt8 = V transposed to
+    [B, Hkv, D, Nk] (keys fastest), the layout attn_fwd_fp8 reads; v8 is
+    [B, Hkv, Nk, D]."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(w.seed + 50000)
+
+    def draw(shape):
+        x = torch.randn(shape, generator=gen, dtype=torch.float32, device=device)
+        if w.sigma != 1.0:
+            x.mul_(w.sigma)
+        return x.clamp_(-448.0, 448.0).to(torch.float8_e4m3fn)
+
+    q8 = draw((w.B, w.Hq, w.Nq, w.D))
+    k8 = draw((w.B, w.Hkv, w.Nk, w.D))
+    v8 = draw((w.B, w.Hkv, w.Nk, w.D))
+    vt8 = v8.transpose(2, 3).contiguous()
+    return q8, k8, v8, vt8
+
+
 def sample_rows(w: Workload, n: int, seed: int = 7) -> torch.Tensor:
     """Flat query-row indices ``(b*Hq + h)*Nq + i`` to check on a large
     workload: ``n`` uniform draws from a fixed seed, plus row 0 and row

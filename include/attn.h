@@ -94,6 +94,34 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, i
              int Hkv, int Nq, int Nk, int D, int causal, float scale, cudaStream_t stream);
 
 /*
+ * attn_fwd_fp8 -- attention forward on FP8 inputs (the FP8 tensor-core path
+ * named on the page "FlashAttention-3 vs Triton Kernels", introduction and
+ * pipeline diagram).  The real operands are q_scale*Q, k_scale*K and
+ * v_scale*V, where Q, K, V hold E4M3 codes (OCP 8-bit floating point,
+ * no infinities):
+ *
+ *   q  [B, Hq,  Nq, 128] e4m3 codes, contiguous
+ *   k  [B, Hkv, Nk, 128] e4m3 codes, contiguous
+ *   vt [B, Hkv, 128, Nk] e4m3 codes: V transposed, keys fastest
+ *   o  [B, Hq,  Nq, 128] bf16, written
+ *   lse [B, Hq, Nq]      fp32, written (natural log of sum_j exp(s_j))
+ *
+ * with s_j = scale * q_scale * k_scale * <Q_i, K_j> and the mask and head
+ * grouping of attn_fwd.  Numerics: S and the softmax statistics are fp32;
+ * the softmax weights are rounded to E4M3 (after multiplying by 2^6, which
+ * keeps the weights of interest out of the subnormal range) for the
+ * FP8 P*V product, accumulated in fp32; the normaliser is summed from the
+ * unrounded fp32 weights.  O is rounded to bf16.
+ *
+ * Limits: D == 128; Nk % 16 == 0 (V^T rows start on 16-byte boundaries);
+ * scale, q_scale, k_scale, v_scale finite and >= 0; the other limits and
+ * the return codes of attn_fwd.
+ */
+int attn_fwd_fp8(const void *q, const void *k, const void *vt, void *o, float *lse, int B, int Hq,
+                 int Hkv, int Nq, int Nk, int D, int causal, float scale, float q_scale,
+                 float k_scale, float v_scale, cudaStream_t stream);
+
+/*
  * attn_decode_splitkv -- split-KV decode of one query row per (batch, head).
  *
  *   q       [B, Hq, D]       bf16, contiguous

@@ -112,3 +112,16 @@ def test_decode_graph_validation(lib):
     assert h.value is None  # nothing handed out on failure
     assert lib.attn_decode_graph_launch(None, None) == -1
     assert lib.attn_decode_graph_destroy(None) == 0
+
+
+def test_fwd_fp8_validation(lib):
+    A = ALIGNED
+    args = (1, 2, 1, 128, 256, 128, 0)
+    assert lib.attn_fwd_fp8(0, A, A, A, A, *args, 0.1, 1.0, 1.0, 1.0, None) == -1
+    assert lib.attn_fwd_fp8(A, A, A, A, A, 1, 2, 1, 128, 250, 128, 0, 0.1, 1.0, 1.0, 1.0,
+                            None) == -3  # Nk % 16
+    assert lib.attn_fwd_fp8(A, A, A, A, A, 1, 2, 1, 128, 256, 64, 0, 0.1, 1.0, 1.0, 1.0,
+                            None) == -3  # D
+    assert lib.attn_fwd_fp8(A, A, A, A, A, *args, 0.1, float("nan"), 1.0, 1.0, None) == -3
+    assert lib.attn_fwd_fp8(A, A, A, A, A, *args, 0.1, 1.0, 1.0, -2.0, None) == -3
+    assert lib.attn_fwd_fp8(A, A, A + 4, A, A, *args, 0.1, 1.0, 1.0, 1.0, None) == -2
