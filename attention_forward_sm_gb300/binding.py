@@ -20,7 +20,8 @@ ATTN_STATUS = {
     -4: "ATTN_ERR_DEVICE", -5: "ATTN_ERR_LAUNCH", -6: "ATTN_ERR_ALLOC", -7: "ATTN_ERR_TMA",
     -8: "ATTN_ERR_CUDA", -9: "ATTN_ERR_SCRATCH",
 }
-EXPORTED = ["attn_fwd", "attn_fwd_fp8", "attn_decode_splitkv", "attn_decode_splitkv_noalloc",
+EXPORTED = ["attn_fwd", "attn_fwd_fp8", "attn_fwd_host", "attn_fwd_host_workspace_bytes",
+            "attn_decode_splitkv", "attn_decode_splitkv_noalloc",
             "attn_status_string", "attn_get_device_error", "attn_decode_workspace_bytes",
             "attn_selftest_wait_timeout", "attn_decode_splitkv_states", "attn_combine_states",
             "attn_decode_graph_create", "attn_decode_graph_launch", "attn_decode_graph_destroy"]
@@ -50,6 +51,10 @@ def load(path: str = LIB_PATH):
         vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
         lib.attn_fwd.restype = i
+        lib.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+        lib.attn_fwd_host.restype = i
+        lib.attn_fwd_host_workspace_bytes.argtypes = [i, i, i, i, i, i]
+        lib.attn_fwd_host_workspace_bytes.restype = ctypes.c_longlong
         lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, f, f, f, vp]
         lib.attn_fwd_fp8.restype = i
         lib.attn_decode_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, vp]
@@ -111,6 +116,19 @@ def attn_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, causal, scale, stream=None)
     _check(load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(Hq),
                            int(Hkv), int(Nq), int(Nk), int(D), int(bool(causal)), float(scale),
                            _stream(stream)))
+
+
+def attn_fwd_host(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, causal, scale, stream=None) -> None:
+    """``attn_fwd_host`` of include/attn.h: host (CPU, ideally pinned) tensors
+    in and out; asynchronous on the stream."""
+    _check(load().attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(Hq),
+                                int(Hkv), int(Nq), int(Nk), int(D), int(bool(causal)),
+                                float(scale), _stream(stream)))
+
+
+def attn_fwd_host_workspace_bytes(B, Hq, Hkv, Nq, Nk, D) -> int:
+    return int(load().attn_fwd_host_workspace_bytes(int(B), int(Hq), int(Hkv), int(Nq), int(Nk),
+                                                    int(D)))
 
 
 def attn_fwd_fp8(q, k, vt, o, lse, B, Hq, Hkv, Nq, Nk, D, causal, scale, q_scale, k_scale,

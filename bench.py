@@ -500,26 +500,21 @@ def run_e2e(args, attn, W, wp, wd, dev, world):
     dhq, dhk, dhv = W.make_inputs(wd, dev)
     host_din = [t.to("cpu").pin_memory() for t in (dhq, dhk, dhv)]
     del hq, hk, hv, dhq, dhk, dhv
-    dev_in = [torch.empty_like(t, device=dev) for t in host_in]
     dev_din = [torch.empty_like(t, device=dev) for t in host_din]
-    o = torch.empty_like(dev_in[0])
-    lse = torch.empty((wp.B, wp.Hq, wp.Nq), dtype=torch.float32, device=dev)
     do = torch.empty_like(dev_din[0])
     dlse = torch.empty((wd.B, wd.Hq), dtype=torch.float32, device=dev)
-    h_o = torch.empty(o.shape, dtype=o.dtype, **pin)
-    h_lse = torch.empty(lse.shape, dtype=lse.dtype, **pin)
+    h_o = torch.empty(host_in[0].shape, dtype=host_in[0].dtype, **pin)
+    h_lse = torch.empty((wp.B, wp.Hq, wp.Nq), dtype=torch.float32, **pin)
     h_do = torch.empty(do.shape, dtype=do.dtype, **pin)
     h_dlse = torch.empty(dlse.shape, dtype=dlse.dtype, **pin)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
 
     def step(record=None):
-        for d, h in zip(dev_in, host_in):
-            d.copy_(h, non_blocking=True)
-        attn.attn_fwd(dev_in[0], dev_in[1], dev_in[2], o, lse, wp.B, wp.Hq, wp.Hkv, wp.Nq, wp.Nk,
-                      wp.D, wp.causal, wp.scale, sh)
-        h_o.copy_(o, non_blocking=True)
-        h_lse.copy_(lse, non_blocking=True)
+        # prefill: host buffers in and out through attn_fwd_host, whose copies
+        # in, compute and copies out overlap unit by unit
+        attn.attn_fwd_host(host_in[0], host_in[1], host_in[2], h_o, h_lse, wp.B, wp.Hq, wp.Hkv,
+                           wp.Nq, wp.Nk, wp.D, wp.causal, wp.scale, sh)
         if record is not None:
             record.record(stream)
         for d, h in zip(dev_din, host_din):
@@ -551,7 +546,9 @@ def run_e2e(args, attn, W, wp, wd, dev, world):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": (pf + dec) / K,
             "decode_gbs": world * K * wd.decode_bytes() / (dec * 1e-3) / 1e9,
-            "steps": K, "path": "pinned host -> device copies, attn_fwd, attn_decode_splitkv, "
+            "steps": K, "path": "prefill: attn_fwd_host on pinned host buffers (copies in, "
+                                "compute and copies out pipelined per (batch, KV-head block)); "
+                                "decode: pinned host -> device copies, attn_decode_splitkv, "
                                 "device -> pinned host copies (C ABI via ctypes)"}
 
 

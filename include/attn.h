@@ -94,6 +94,34 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, i
              int Hkv, int Nq, int Nk, int D, int causal, float scale, cudaStream_t stream);
 
 /*
+ * attn_fwd_host -- attn_fwd on operands in host memory (pinned memory,
+ * e.g. from cudaHostAlloc, lets the copies run asynchronously and at full
+ * speed; pageable memory works but the copies then block the host).
+ *
+ * Same arguments, layouts, numerics and results as attn_fwd, but q, k, v, o
+ * and lse are HOST pointers.  The work is cut into units of whole
+ * (batch, KV-head block) slices -- the smallest block of KV heads whose
+ * query tiles fill the GPU about four times -- and pipelined through two
+ * device slots: the inputs of unit u are copied in on one library-owned
+ * stream while unit u-1 computes on `stream` and unit u-2's outputs are
+ * copied out on another, so a call costs about the largest of the three
+ * instead of their sum.  Results are bit-identical to attn_fwd on device
+ * copies of the inputs.
+ *
+ * Asynchronous: returns once everything is enqueued; `stream` completes
+ * only after the last output byte has reached o/lse.  The host buffers must
+ * stay valid until then, and must not be written (inputs) or read (outputs)
+ * before.  The device slots (attn_fwd_host_workspace_bytes) are taken with
+ * cudaMallocAsync on `stream` and freed the same way.  Returns the
+ * validation errors of attn_fwd (before any copy), ATTN_ERR_ALLOC, or
+ * ATTN_ERR_CUDA if a copy, event or stream call fails.
+ */
+int attn_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
+                  int Hkv, int Nq, int Nk, int D, int causal, float scale, cudaStream_t stream);
+/* Device bytes attn_fwd_host takes for its two slots (0 for invalid sizes). */
+long long attn_fwd_host_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int D);
+
+/*
  * attn_fwd_fp8 -- attention forward on FP8 inputs (the FP8 tensor-core path
  * named on the page "FlashAttention-3 vs Triton Kernels", introduction and
  * pipeline diagram).  The real operands are q_scale*Q, k_scale*K and

@@ -125,3 +125,21 @@ def test_fwd_fp8_validation(lib):
     assert lib.attn_fwd_fp8(A, A, A, A, A, *args, 0.1, float("nan"), 1.0, 1.0, None) == -3
     assert lib.attn_fwd_fp8(A, A, A, A, A, *args, 0.1, 1.0, 1.0, -2.0, None) == -3
     assert lib.attn_fwd_fp8(A, A, A + 4, A, A, *args, 0.1, 1.0, 1.0, 1.0, None) == -2
+
+
+def test_fwd_host_validation(lib):
+    A = ALIGNED
+    assert lib.attn_fwd_host(0, A, A, A, A, 1, 2, 2, 8, 8, 64, 0, 0.1, None) == -1
+    assert lib.attn_fwd_host(A, A, A, A, A, 1, 3, 2, 8, 8, 64, 0, 0.1, None) == -3
+    assert lib.attn_fwd_host(A, A, A, A, A, 1, 2, 2, 8, 8, 96, 0, 0.1, None) == -3
+    assert lib.attn_fwd_host(A, A, A, A, A, 1, 2, 2, 8, 8, 64, 0, -1.0, None) == -3
+
+
+def test_fwd_host_workspace_plan(lib):
+    # B8 Hq=Hkv=32 N8192 D128: 32 q-tile pairs per head -> 19 heads fill four
+    # waves of 152 CTAs -> two blocks of 16 heads; a slot holds q, k, v, o of
+    # 16 heads and their lse
+    per_head = 8192 * 128 * 2
+    slot = 4 * 16 * per_head + 16 * 8192 * 4
+    assert attn.attn_fwd_host_workspace_bytes(8, 32, 32, 8192, 8192, 128) == 2 * slot
+    assert attn.attn_fwd_host_workspace_bytes(0, 32, 32, 8192, 8192, 128) == 0
