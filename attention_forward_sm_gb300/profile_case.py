@@ -1,6 +1,6 @@
 """Run one library kernel on a small named case, for profilers (ncu).
 
-    python -m attention_forward_sm_gb300.profile_case fwd|fwd-causal|decode [--iters N]
+    python -m attention_forward_sm_gb300.profile_case fwd|fwd-causal|fwd-fp8|decode [--iters N]
 
 Each case keeps every input tensor above the 129 MB L2 but the whole case
 under ~1 GB of device memory, so a multi-pass ncu capture of one launch
@@ -23,7 +23,10 @@ CASES = {
     "fwd-causal": W.custom(4, 32, 32, 4096, 4096, 128, True, seed_index=901),
     # decode: 8 x 8 KV heads x 16384 keys x 128: 268 MB per cache
     "decode": W.custom(8, 32, 8, 1, 16384, 128, False, seed_index=902, decode=True, nsplit=32),
+    # FP8 prefill: the fwd shape with E4M3 inputs (67 MB per tensor, 134 MB for O)
+    "fwd-fp8": W.custom(4, 32, 32, 4096, 4096, 128, False, seed_index=903),
 }
+FP8 = {"fwd-fp8"}
 
 
 def main():
@@ -33,9 +36,20 @@ def main():
     ap.add_argument("--warmup", type=int, default=2)
     args = ap.parse_args()
     w = CASES[args.case]
-    q, k, v = W.make_inputs(w, "cuda")
-    o = torch.empty_like(q)
-    if w.decode:
+    if args.case in FP8:
+        q, k, _, v = W.make_inputs_fp8(w, "cuda")  # v: V transposed
+        o = torch.empty(q.shape, dtype=torch.bfloat16, device="cuda")
+    else:
+        q, k, v = W.make_inputs(w, "cuda")
+        o = torch.empty_like(q)
+    if args.case in FP8:
+        lse = torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device="cuda")
+        sc = W.FP8_SCALES
+
+        def call():
+            attn.attn_fwd_fp8(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.D, w.causal,
+                              w.scale, sc["q"], sc["k"], sc["v"])
+    elif w.decode:
         lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device="cuda")
 
         def call():
