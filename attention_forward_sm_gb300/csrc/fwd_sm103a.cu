@@ -182,11 +182,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---- work unit: (batch*head, pair of 128-row query tiles)
+  // ---- work unit: (batch*head, pair of 128-row query tiles).  Non-causal:
+  // head-major.  Causal: heads in groups of p.group_heads (sized on the host
+  // so a group's K/V stays in L2); inside a group all units longest first,
+  // so the block scheduler ends every group, and the grid, on short units.
   const int nqb = (p.Nq + 2 * kBM - 1) / (2 * kBM);
-  int qblk = static_cast<int>(blockIdx.x % nqb);
-  const int bh = static_cast<int>(blockIdx.x / nqb);
-  if (p.causal) qblk = nqb - 1 - qblk;  // longest rows first
+  int qblk, bh;
+  if (p.causal) {
+    const int BH = p.B * p.Hq;
+    const int per_group = p.group_heads * nqb;
+    const int g = static_cast<int>(blockIdx.x / per_group);
+    const int idx = static_cast<int>(blockIdx.x % per_group);
+    const int heads = min(p.group_heads, BH - g * p.group_heads);
+    qblk = nqb - 1 - idx / heads;
+    bh = g * p.group_heads + idx % heads;
+  } else {
+    qblk = static_cast<int>(blockIdx.x % nqb);
+    bh = static_cast<int>(blockIdx.x / nqb);
+  }
   const int q_base = qblk * 2 * kBM;
   const int G = p.Hq / p.Hkv;
   const int bhkv = (bh / p.Hq) * p.Hkv + (bh % p.Hq) / G;
@@ -546,8 +559,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Causal unit order: query heads per group, whole KV-head groups, so that
+// the group's K and V (read by every unit of its heads) take at most about
+// a third of the 129 MB L2.
+int causal_group_heads(const FwdParams& p) {
+  const int G = p.Hq / p.Hkv;
+  const double kv_bytes = 2.0 * p.Nk * p.D * (p.fp8 ? 1 : 2);  // K and V of one KV head
+  int kv_heads = static_cast<int>(40.0e6 / kv_bytes);
+  kv_heads = max(1, min(kv_heads, p.B * p.Hkv));
+  return kv_heads * G;
+}
+
 template <int D, bool kFp8>
-cudaError_t launch_d(const FwdParams& p, cudaStream_t stream) {
+cudaError_t launch_d(const FwdParams& p_in, cudaStream_t stream) {
+  FwdParams p = p_in;
+  p.group_heads = causal_group_heads(p);
   using C = Cfg<D, kFp8>;
   // the shared-memory opt-in is a per-device property of the function
   static bool attr_done[64] = {};

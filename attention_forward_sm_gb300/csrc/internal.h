@@ -27,6 +27,7 @@ struct FwdParams {
   int B, Hq, Hkv, Nq, Nk, D;
   int causal;
   int fp8;             // e4m3 Q, K, V^T
+  int group_heads;     // causal unit order: query heads per group (a multiple of Hq/Hkv)
   float scale_log2;    // scale * log2(e) (FP8: times q_scale * k_scale)
   float o_scale;       // O multiplier (FP8: v_scale; bf16: 1)
   unsigned int* err;   // device error word
