@@ -115,6 +115,24 @@ def test_full_size_sampled(name):
         assert torch.equal(o[:, :, 0, :], v0)
 
 
+def test_causal_unit_groups_with_a_partial_last_group():
+    """Causal units run in groups of whole KV heads sized to L2 (K+V of
+    16.8 MB per KV head at Nk = 32768 gives two KV heads per group); with
+    three KV heads the last group holds one.  Every row of every head is
+    computed: sampled rows of all six query heads against the oracle, and
+    row 0 of each head is V[0] exactly."""
+    w = W.custom(1, 6, 3, 32768, 32768, 128, True, seed_index=1200)
+    q, k, v = W.make_inputs(w, "cuda")
+    o, lse = run_prefill(w, q, k, v)
+    rows = W.sample_rows(w, 1024)
+    o_ref, lse_ref = oracle_prefill(w, q, k, v, rows.numpy())
+    check(o.reshape(-1, w.D)[rows.cuda()], lse.reshape(-1)[rows.cuda()], o_ref, lse_ref,
+          "causal groups")
+    heads = set((rows // w.Nq).tolist())
+    assert heads == set(range(w.B * w.Hq))
+    assert torch.equal(o[:, :, 0, :], v[:, :, 0, :].repeat_interleave(2, dim=1))
+
+
 def test_scale_zero_is_uniform():
     """scale = 0: every visible key has the same weight (oracle and closed form)."""
     w = W.custom(1, 2, 2, 300, 300, 128, True, seed_index=501)
