@@ -17,6 +17,8 @@
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
+#include <atomic>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -417,16 +419,16 @@ template <int D, int GT>
 cudaError_t launch_split_t(const DecodeParams& p, cudaStream_t stream) {
   constexpr int smem = split_smem_bytes<D>();
   // the shared-memory opt-in is a per-device property of the function
-  static bool attr_done[64] = {};
+  static std::atomic<bool> attr_done[64];  // zero-initialised: false
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_done[dev]) {
+  if (!attr_done[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(decode_split_kernel<D, GT>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
+    attr_done[dev].store(true, std::memory_order_release);
   }
   const int G = p.Hq / p.Hkv;
   dim3 grid(p.nsplit, p.Hkv * (G / GT), p.B);

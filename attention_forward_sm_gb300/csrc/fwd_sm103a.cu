@@ -35,6 +35,8 @@
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
+#include <atomic>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -576,16 +578,16 @@ cudaError_t launch_d(const FwdParams& p_in, cudaStream_t stream) {
   p.group_heads = causal_group_heads(p);
   using C = Cfg<D, kFp8>;
   // the shared-memory opt-in is a per-device property of the function
-  static bool attr_done[64] = {};
+  static std::atomic<bool> attr_done[64];  // zero-initialised: false
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_done[dev]) {
+  if (!attr_done[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(attn_fwd_kernel<D, kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
+    attr_done[dev].store(true, std::memory_order_release);
   }
   const long long nqb = (p.Nq + 2 * kBM - 1) / (2 * kBM);
   const long long grid = nqb * p.B * p.Hq;
