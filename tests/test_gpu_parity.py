@@ -133,6 +133,51 @@ def test_causal_unit_groups_with_a_partial_last_group():
     assert torch.equal(o[:, :, 0, :], v[:, :, 0, :].repeat_interleave(2, dim=1))
 
 
+def test_more_than_2_31_elements():
+    """Tensors of more than 2^31 elements (B2 H32 N266240 D128 causal: 4.4 GB each):
+    every offset the kernel forms stays in range.  Sampled rows from both
+    batch entries against the oracle, and causal row 0 of every head."""
+    w = W.custom(2, 32, 32, 266240, 266240, 128, True, seed_index=1300)
+    assert w.B * w.Hq * w.Nq * w.D > 2 ** 31
+    q, k, v = W.make_inputs(w, "cuda")
+    o, lse = run_prefill(w, q, k, v)
+    g = torch.Generator().manual_seed(11)
+    total = w.B * w.Hq * w.Nq
+    rows = torch.unique(torch.cat([torch.randint(0, total, (192,), generator=g),
+                                   torch.tensor([total - 1, total // 2 - 1, total // 2])]))
+    o_ref, lse_ref = oracle_prefill(w, q, k, v, rows.numpy())
+    check(o.reshape(-1, w.D)[rows.cuda()], lse.reshape(-1)[rows.cuda()], o_ref, lse_ref,
+          "2^31+ elements")
+    assert torch.equal(o[:, :, 0, :], v[:, :, 0, :])
+    del q, k, v, o, lse
+    torch.cuda.empty_cache()
+
+
+RANDOM_SHAPES = 24
+
+
+@pytest.mark.parametrize("case", range(RANDOM_SHAPES))
+def test_random_shapes(case):
+    """Seeded random shapes over the supported space: B 1-3, KV heads 1-4,
+    group size 1-4, Nq and Nk 1-1500, D 64 or 128, causal or not, scale in
+    [0, 0.3]."""
+    g = torch.Generator().manual_seed(4000 + case)
+    ri = lambda lo, hi: int(torch.randint(lo, hi + 1, (1,), generator=g))
+    Hkv = ri(1, 4)
+    B, Hq, Nq, Nk = ri(1, 3), Hkv * ri(1, 4), ri(1, 1500), ri(1, 1500)
+    D, causal = (64, 128)[ri(0, 1)], bool(ri(0, 1))
+    scale = float(torch.rand(1, generator=g)) * 0.3
+    w = W.custom(B, Hq, Hkv, Nq, Nk, D, causal, seed_index=4100 + case)
+    q, k, v = (t.cuda() for t in W.make_inputs(w, "cpu"))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device="cuda")
+    attn.attn_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, causal, scale)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle_prefill(w, q, k, v, scale=scale)
+    check(o, lse, o_ref.reshape(o.shape), lse_ref.reshape(lse.shape),
+          f"B{B} Hq{Hq} Hkv{Hkv} Nq{Nq} Nk{Nk} D{D} causal{causal} scale{scale:.3f}")
+
+
 def test_scale_zero_is_uniform():
     """scale = 0: every visible key has the same weight (oracle and closed form)."""
     w = W.custom(1, 2, 2, 300, 300, 128, True, seed_index=501)
