@@ -271,6 +271,24 @@ def test_decode_sweep(shape):
     check(o, lse, o_ref.reshape(o.shape), lse_ref.reshape(lse.shape), str(shape))
 
 
+@pytest.mark.parametrize("case", range(16))
+def test_decode_random_shapes(case):
+    """Seeded random decode shapes: B 1-4, KV heads 1-8, group size 1-12 (odd
+    ones included), Nk 1-20000, D 64 or 128, nsplit 1..min(Nk, 64)."""
+    g = torch.Generator().manual_seed(5000 + case)
+    ri = lambda lo, hi: int(torch.randint(lo, hi + 1, (1,), generator=g))
+    B, Hkv, G = ri(1, 4), ri(1, 8), ri(1, 12)
+    Nk, D = ri(1, 20000), (64, 128)[ri(0, 1)]
+    nsplit = ri(1, min(Nk, 64))
+    w = W.custom(B, Hkv * G, Hkv, 1, Nk, D, False, seed_index=5100 + case, decode=True,
+                 nsplit=nsplit)
+    q, k, v = (t.cuda() for t in W.make_inputs(w, "cpu"))
+    o, lse = run_decode(w, q, k, v, nsplit)
+    o_ref, lse_ref = oracle_decode(w, q, k, v)
+    check(o, lse, o_ref.reshape(o.shape), lse_ref.reshape(lse.shape),
+          f"B{B} Hq{Hkv * G} Hkv{Hkv} Nk{Nk} D{D} nsplit{nsplit}")
+
+
 def test_decode_split_invariance():
     """Different nsplit give the same result (LSE recombination), within tolerance."""
     w = W.custom(2, 8, 2, 1, 5000, 128, False, seed_index=700, decode=True, nsplit=1)
