@@ -223,8 +223,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ms.abort_flag = 0;
     fence_mbar_init();
-    tma_prefetch_desc(&p.tmap_q);
-    tma_prefetch_desc(&p.tmap_k);
+    // The Q tiles and the first K tile start loading now, before the CTA-wide
+    // barrier and the TMEM allocation: they are the first MMA's operands.
+    mbar_arrive_expect_tx(&ms.q_full, 2 * C::kTileBytes);
+    for (int t = 0; t < 2; ++t)
+      for (int ch = 0; ch < C::kChunks; ++ch)
+        tma_load_3d(smem + C::kOffQ + t * C::kTileBytes + ch * (kBM * 128), &p.tmap_q,
+                    &ms.q_full, ch * C::kAtomElems, q_base + t * kBM, bh,
+                    l2_policy_evict_first());
+    mbar_arrive_expect_tx(&ms.kv_full[0], C::kTileBytes);
+    for (int ch = 0; ch < C::kChunks; ++ch)
+      tma_load_3d(smem + C::kOffKV + ch * (kBM * 128), &p.tmap_k, &ms.kv_full[0],
+                  ch * C::kAtomElems, 0, bhkv, l2_policy_evict_last());
     tma_prefetch_desc(&p.tmap_v);
     tma_prefetch_desc(&p.tmap_o);
   }
@@ -432,15 +442,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // =====================================================================
     reg_dealloc<kRegOther>();
     if (lane == 0) {
-      const uint64_t pol_q = l2_policy_evict_first();
       const uint64_t pol_kv = l2_policy_evict_last();
-      mbar_arrive_expect_tx(&ms.q_full, 2 * C::kTileBytes);
-      for (int t = 0; t < 2; ++t)
-        for (int ch = 0; ch < C::kChunks; ++ch)
-          tma_load_3d(smem + C::kOffQ + t * C::kTileBytes + ch * (kBM * 128), &p.tmap_q,
-                      &ms.q_full, ch * C::kAtomElems, q_base + t * kBM, bh, pol_q);
-      int issued = 0;
-      for (int it = 0; it < 2 * n_kv; ++it) {
+      // Q and K_0 were issued during setup
+      int issued = 1;
+      for (int it = 1; it < 2 * n_kv; ++it) {
         const int s = it % C::kStages;
         const uint32_t ph = static_cast<uint32_t>(it / C::kStages) & 1u;
         if (!mbar_wait(&ms.kv_empty[s], ph ^ 1u, abort_flag, p.err, kErrWaitLoad, lim)) break;
