@@ -345,7 +345,9 @@ def run_gpu(args):
         q_h, k_h, v_h = q.cpu(), k.cpu(), v.cpu()
         dt, fl, threads, desc = time_oracle(wp, q_h, k_h, v_h, 32768)
         cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-               "sample": desc, "seconds": dt}
+               "sample": desc, "seconds": dt,
+               # the whole workload at the sample's rate (every row costs the same)
+               "extrapolated_full_workload_seconds": dt * wp.flops() / fl}
 
     line = {
         "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
