@@ -18,7 +18,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libattn.so")
-SOURCES = ["api.cu", "fwd_sm103a.cu", "decode_sm103a.cu", "decode_noalloc.cu", "decode_graph.cu", "host_pipeline.cu"]
+SOURCES = ["api.cu", "fwd_sm103a.cu", "decode_sm103a.cu", "decode_noalloc.cu", "decode_graph.cu",
+           "decode_scratch.cu", "host_pipeline.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
          "--expt-relaxed-constexpr", f"-I{INCLUDE}"]

@@ -274,32 +274,13 @@ int attn_fwd_fp8(const void* q, const void* k, const void* vt, void* o, float* l
 }
 
 // Split + combine with stream-ordered scratch for the partial states.
-static int decode_with_scratch(DecodeParams& p, cudaStream_t stream) {
-  if (int rc = decode_bind_device(&p)) return rc;
-  size_t o_bytes = 0;
-  const size_t bytes = decode_scratch_bytes(p, &o_bytes);
-  void* ws = nullptr;
-  if (cudaMallocAsync(&ws, bytes, stream) != cudaSuccess) {
-    cudaGetLastError();
-    return ATTN_ERR_ALLOC;
-  }
-  p.ws_o = static_cast<float*>(ws);
-  p.ws_lse = reinterpret_cast<float*>(static_cast<char*>(ws) + o_bytes);
-  int rc = ATTN_OK;
-  if (launch_decode_split(p, stream) != cudaSuccess ||
-      launch_decode_combine(p, stream) != cudaSuccess)
-    rc = ATTN_ERR_LAUNCH;
-  if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == ATTN_OK) rc = ATTN_ERR_CUDA;
-  return rc;
-}
-
 int attn_decode_splitkv(const void* q, const void* kcache, const void* vcache, void* o, float* lse,
                         int B, int Hq, int Hkv, int Nk, int D, int nsplit, cudaStream_t stream) {
   if (!o) return ATTN_ERR_NULL;
   DecodeParams p;
   if (int rc = decode_prepare(q, kcache, vcache, o, nullptr, lse, B, Hq, Hkv, Nk, D, nsplit, &p))
     return rc;
-  return decode_with_scratch(p, stream);
+  return decode_with_cached_scratch(p, stream);
 }
 
 int attn_decode_splitkv_states(const void* q, const void* kcache, const void* vcache,
@@ -310,7 +291,7 @@ int attn_decode_splitkv_states(const void* q, const void* kcache, const void* vc
   if (int rc =
           decode_prepare(q, kcache, vcache, nullptr, o_state, lse, B, Hq, Hkv, Nk, D, nsplit, &p))
     return rc;
-  return decode_with_scratch(p, stream);
+  return decode_with_cached_scratch(p, stream);
 }
 
 int attn_combine_states(const float* part_o, const float* part_lse, void* o, float* lse,

@@ -70,6 +70,10 @@ int decode_bind_device(DecodeParams* p);
 // outputs' share (the partial lse follow them).
 size_t decode_scratch_bytes(const DecodeParams& p, size_t* o_bytes);
 
+// Binds the device, takes the partial-state scratch from the per-stream cache
+// (or, during stream capture, from the stream-ordered allocator) and queues
+// the split and combine kernels.  Returns an ATTN_* status.
+int decode_with_cached_scratch(DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_decode_split(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream);
 bool decode_supported(int G, int D);

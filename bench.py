@@ -380,8 +380,9 @@ def time_other_workloads(attn, W, dev, peak_tflops, calls=3):
     returns {name: {...}} with TFLOP/s (causal flops halved)."""
     import torch
     out = {}
-    for name in ("causal", "long_gqa", "tiny"):
-        w = W.WORKLOADS[name]
+    d64 = W.custom(8, 32, 32, 8192, 8192, 64, False, seed_index=960)
+    for name in ("causal", "long_gqa", "tiny", "d64"):
+        w = d64 if name == "d64" else W.WORKLOADS[name]
         q, k, v = W.make_inputs(w, dev)
         o = torch.empty_like(q)
         lse = torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device=dev)
@@ -462,11 +463,15 @@ def time_decode_graph(attn, W, dev, wd, calls=200):
         def direct():
             attn.attn_decode_splitkv(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.Nk, w.D, w.nsplit, sh)
 
+        def noalloc():
+            attn.attn_decode_splitkv_noalloc(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.Nk, w.D,
+                                             w.nsplit, sh)
+
         def graph():
             attn.attn_decode_graph_launch(g.handle, sh)
 
         res = {"workload": w.label(), "calls": n}
-        for label, fn in (("direct", direct), ("graph", graph)):
+        for label, fn in (("direct", direct), ("noalloc", noalloc), ("graph", graph)):
             for _ in range(5):
                 fn()
             torch.cuda.synchronize(dev)

@@ -163,10 +163,15 @@ int attn_fwd_fp8(const void *q, const void *k, const void *vt, void *o, float *l
  * empty); each chunk yields a partial output normalised by its own softmax
  * denominator plus its lse, and a second kernel recombines them:
  *   L = ln sum_c exp(lse_c),   O = sum_c exp(lse_c - L) O_c.
- * The partial states live in scratch memory the library takes from the
- * stream-ordered allocator on `stream` and frees on `stream` after the
- * combine (B*Hq*nsplit*(D+1)*4 bytes), so calls on different streams do not
- * share scratch.
+ * The partial states (B*Hq*nsplit*(D+1)*4 bytes) live in a device buffer the
+ * library keeps per stream: on each device it remembers the last 8 streams
+ * it decoded on, each with one buffer taken from the stream-ordered
+ * allocator, grown when a call needs more and otherwise reused, so a
+ * repeated decode step allocates nothing.  Each use waits (on the GPU) for
+ * the buffer's previous use, so calls never share scratch while running.
+ * The buffers stay allocated until the process exits or their entry passes
+ * to another stream.  During stream capture a call allocates its scratch on
+ * the stream and frees it after the combine instead (the graph owns it).
  *
  * Limits: B, Hq, Hkv, Nk >= 1; Hq % Hkv == 0; D in {64, 128};
  * 1 <= nsplit <= Nk; B <= 65535; pointers 16-byte aligned.
