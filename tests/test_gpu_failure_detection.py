@@ -1,7 +1,6 @@
 """Failure detection without a GPU fault: a kernel whose pipeline wait can
 never complete gives up after its time limit, reports it through the device
 error word, and the CUDA context stays usable for the next call."""
-import math
 
 import numpy as np
 import pytest
