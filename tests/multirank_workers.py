@@ -51,3 +51,51 @@ def sp_decode_worker(rank, world, port, B, Hq, Hkv, Nk, D, seed):
     assert np.abs(lse - lse_ref).max() < 1e-5
     # the naive sum of the per-rank outputs is not attention (denominator pitfall)
     dist.destroy_process_group()
+
+
+def sp_decode_failure_worker(rank, world, port, fail_rank, results, stall_s=0.0):
+    """The sequence-parallel decode with one rank that fails before the state
+    exchange -- at once, or after stalling `stall_s` seconds without joining
+    the collective: the others must leave the all-gather with an error within
+    the process group's short timeout (reported through `results`), not
+    hang."""
+    import datetime
+    import time
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world,
+                            timeout=datetime.timedelta(seconds=5))
+    import oracle
+    from attention_forward_sm_gb300 import sp_decode
+    B, Hq, Hkv, Nk, D = 1, 4, 2, 64, 16
+    g = torch.Generator().manual_seed(7)
+    q = torch.randn(B, Hq, D, generator=g).to(torch.bfloat16)
+    k = torch.randn(B, Hkv, Nk, D, generator=g).to(torch.bfloat16)
+    v = torch.randn(B, Hkv, Nk, D, generator=g).to(torch.bfloat16)
+    s0, s1 = sp_decode.shard_range(Nk, world, rank)
+    ks, vs = k[:, :, s0:s1].contiguous(), v[:, :, s0:s1].contiguous()
+    scale = 1.0 / math.sqrt(D)
+
+    def local_states(q_, k_, v_, nsplit):
+        if rank == fail_rank:
+            time.sleep(stall_s)
+            raise RuntimeError("injected failure on the host before the exchange")
+        o, l = oracle.attn_rows(q_, k_, v_, B, Hq, Hkv, 1, k_.shape[2], D, False, scale)
+        return torch.from_numpy(o).float(), torch.from_numpy(l).float()
+
+    def combine(part_o, part_lse):
+        return oracle.combine(part_o.double().numpy(), part_lse.double().numpy())
+
+    t0 = time.monotonic()
+    code = 0
+    try:
+        sp_decode.sp_flash_decode(q, ks, vs, 4, local_states=local_states, combine=combine)
+        results.put((rank, "completed", time.monotonic() - t0))
+    except Exception as e:  # noqa: BLE001 - any error is the detection we want
+        results.put((rank, type(e).__name__, time.monotonic() - t0))
+        if rank == fail_rank:
+            code = 3  # the failing rank dies without a clean shutdown
+    # flush the report before the hard exit (the queue's writer is a thread)
+    results.close()
+    results.join_thread()
+    os._exit(code)

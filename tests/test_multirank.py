@@ -45,3 +45,38 @@ def test_bench_max_over_ranks_gloo():
 def test_sp_flash_decode_gloo(world, Nk):
     mp.spawn(W.sp_decode_worker, args=(world, _free_port(), 2, 8, 2, Nk, 16, 5 + world),
              nprocs=world, join=True)
+
+
+@pytest.mark.parametrize("world,fail_rank,stall_s", [(2, 1, 0.0), (3, 0, 0.0), (3, 2, 0.0),
+                                                     (2, 0, 12.0)])
+def test_sp_decode_rank_failure_is_detected(world, fail_rank, stall_s):
+    """A rank raises before the state exchange and exits -- at once, or after
+    stalling past the process group's 5 s timeout without joining the
+    all-gather; every other rank gets an error out of the all-gather
+    instead of hanging (a dead peer within ~20 ms, a stalled one at the
+    timeout), and no rank reports a result."""
+    ctx = mp.get_context("spawn")
+    results = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=W.sp_decode_failure_worker,
+                         args=(r, world, port, fail_rank, results, stall_s))
+             for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=60)
+    alive = [p for p in procs if p.is_alive()]
+    for p in alive:
+        p.kill()
+    assert not alive, "a rank hung after a peer failed"
+    got = {}
+    while len(got) < world:
+        r, what, dt = results.get(timeout=10)
+        got[r] = (what, dt)
+    assert got[fail_rank][0] == "RuntimeError"
+    for r in range(world):
+        assert got[r][0] != "completed", got
+        assert got[r][1] < 30.0, got
+        if r != fail_rank and stall_s > 0:
+            assert got[r][1] < stall_s, got  # released by the timeout, not by the exit
+    assert procs[fail_rank].exitcode == 3
