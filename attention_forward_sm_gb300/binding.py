@@ -20,7 +20,7 @@ ATTN_STATUS = {
     -4: "ATTN_ERR_DEVICE", -5: "ATTN_ERR_LAUNCH", -6: "ATTN_ERR_ALLOC", -7: "ATTN_ERR_TMA",
     -8: "ATTN_ERR_CUDA", -9: "ATTN_ERR_SCRATCH",
 }
-EXPORTED = ["attn_fwd", "attn_fwd_fp8", "attn_fwd_host", "attn_fwd_host_workspace_bytes",
+EXPORTED = ["attn_fwd", "attn_fwd_rows", "attn_fwd_fp8", "attn_fwd_host", "attn_fwd_host_workspace_bytes",
             "attn_decode_splitkv", "attn_decode_splitkv_noalloc",
             "attn_status_string", "attn_get_device_error", "attn_decode_workspace_bytes",
             "attn_selftest_wait_timeout", "attn_decode_splitkv_states", "attn_combine_states",
@@ -51,6 +51,8 @@ def load(path: str = LIB_PATH):
         vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
         lib.attn_fwd.restype = i
+        lib.attn_fwd_rows.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, vp]
+        lib.attn_fwd_rows.restype = i
         lib.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
         lib.attn_fwd_host.restype = i
         lib.attn_fwd_host_workspace_bytes.argtypes = [i, i, i, i, i, i]
@@ -116,6 +118,16 @@ def attn_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, causal, scale, stream=None)
     _check(load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(Hq),
                            int(Hkv), int(Nq), int(Nk), int(D), int(bool(causal)), float(scale),
                            _stream(stream)))
+
+
+def attn_fwd_rows(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, causal, q_offset, scale,
+                  stream=None) -> None:
+    """``attn_fwd_rows`` of include/attn.h: ``attn_fwd`` for query rows
+    q_offset .. q_offset+Nq-1 of a longer sequence (the causal mask uses the
+    global row index)."""
+    _check(load().attn_fwd_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(Hq),
+                                int(Hkv), int(Nq), int(Nk), int(D), int(bool(causal)),
+                                int(q_offset), float(scale), _stream(stream)))
 
 
 def attn_fwd_host(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, causal, scale, stream=None) -> None:

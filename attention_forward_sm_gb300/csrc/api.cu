@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
+#include <limits.h>
 #include <math.h>
 #include <stdint.h>
 
@@ -202,10 +203,18 @@ long long attn_decode_workspace_bytes(int B, int Hq, int D, int nsplit) {
 
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
              int Hkv, int Nq, int Nk, int D, int causal, float scale, cudaStream_t stream) {
+  return attn_fwd_rows(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, causal, 0, scale, stream);
+}
+
+int attn_fwd_rows(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                  int Hkv, int Nq, int Nk, int D, int causal, int q_offset, float scale,
+                  cudaStream_t stream) {
   if (!q || !k || !v || !o || !lse) return ATTN_ERR_NULL;
   if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nk < 1 || Hq % Hkv != 0) return ATTN_ERR_SHAPE;
   if (D != 64 && D != 128) return ATTN_ERR_SHAPE;
   if (!isfinite(scale) || scale < 0.f) return ATTN_ERR_SHAPE;
+  // the kernel forms q_offset + (row within the call) + a few tiles in int
+  if (q_offset < 0 || q_offset > INT_MAX - Nq - 1024) return ATTN_ERR_SHAPE;
   const long long nqb = (Nq + 255) / 256;
   if (static_cast<long long>(B) * Hq * nqb >= (1ll << 31)) return ATTN_ERR_SHAPE;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
@@ -226,6 +235,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.Nk = Nk;
   p.D = D;
   p.causal = causal ? 1 : 0;
+  p.q_offset = causal ? q_offset : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.o_scale = 1.f;
   p.err = st->err_word;

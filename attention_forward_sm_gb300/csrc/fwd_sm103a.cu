@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int G = p.Hq / p.Hkv;
   const int bhkv = (bh / p.Hq) * p.Hkv + (bh % p.Hq) / G;
   int n_kv = (p.Nk + kBN - 1) / kBN;
-  if (p.causal) n_kv = min(n_kv, (q_base + 2 * kBM + kBN - 1) / kBN);
+  if (p.causal) n_kv = min(n_kv, (q_base + p.q_offset + 2 * kBM + kBN - 1) / kBN);
 
   // ---- setup: barriers (loader warp), TMEM (MMA warp)
   if (warp == kWarpLoad && lane == 0) {
@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t s_addr = lane_addr + (t ? C::kColS1 : C::kColS0);
     const uint32_t o_addr = lane_addr + (t ? C::kColO1 : C::kColO0);
     const int tile_row0 = q_base + t * kBM;
-    const int vis = p.causal ? min(row + 1, p.Nk) : p.Nk;  // keys [0, vis) visible
+    const int vis = p.causal ? min(row + 1 + p.q_offset, p.Nk) : p.Nk;  // keys [0, vis) visible
     const bool tracer = (warp & 7) == 0 && lane == 0;
     float m = -CUDART_INF_F, l = 0.f;  // l: sum over this thread's half of the row
     bool ok = true;
@@ -287,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tracer) ATTN_TRACE_EV(1, t, j);
       const int kb = j * kBN + c * 64;  // key index of this thread's first column
       const bool need_mask =
-          (j * kBN + kBN > p.Nk) || (p.causal && j * kBN + kBN - 1 > tile_row0);
+          (j * kBN + kBN > p.Nk) || (p.causal && j * kBN + kBN - 1 > tile_row0 + p.q_offset);
       if (need_mask) {
         const int lim_c = vis - kb;  // columns [0, lim_c) valid
 #pragma unroll

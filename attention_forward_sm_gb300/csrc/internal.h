@@ -26,6 +26,7 @@ struct FwdParams {
   float* lse;          // [B, Hq, Nq] fp32
   int B, Hq, Hkv, Nq, Nk, D;
   int causal;
+  int q_offset;        // causal: row i of this call is row q_offset + i of the problem
   int fp8;             // e4m3 Q, K, V^T
   int group_heads;     // causal unit order: query heads per group (a multiple of Hq/Hkv)
   float scale_log2;    // scale * log2(e) (FP8: times q_scale * k_scale)

@@ -94,6 +94,26 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, i
              int Hkv, int Nq, int Nk, int D, int causal, float scale, cudaStream_t stream);
 
 /*
+ * attn_fwd_rows -- attn_fwd on a contiguous block of the query rows of a
+ * longer sequence: row i of this call is row q_offset + i of the problem,
+ * so with causal != 0 it sees keys j <= q_offset + i (k and v hold keys
+ * 0 .. Nk-1 of the whole sequence).  attn_fwd is attn_fwd_rows with
+ * q_offset = 0; without causal masking q_offset has no effect.
+ *
+ * Source: smzdm digest of Zhihu posts, section 5 (SP AllGather attention:
+ * each rank keeps its block of the sequence's queries and gathers the keys
+ * and values of every rank before attending); the Python helper
+ * attention_forward_sm_gb300.sp_prefill does the gather with
+ * torch.distributed and calls this with the rank's row offset.
+ *
+ * Arguments, layouts and limits as attn_fwd, plus 0 <= q_offset <=
+ * INT_MAX - Nq - 1024 (ATTN_ERR_SHAPE otherwise).
+ */
+int attn_fwd_rows(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
+                  int Hkv, int Nq, int Nk, int D, int causal, int q_offset, float scale,
+                  cudaStream_t stream);
+
+/*
  * attn_fwd_host -- attn_fwd on operands in host memory (pinned memory,
  * e.g. from cudaHostAlloc, lets the copies run asynchronously and at full
  * speed; pageable memory works but the copies then block the host).

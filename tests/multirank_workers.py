@@ -99,3 +99,39 @@ def sp_decode_failure_worker(rank, world, port, fail_rank, results, stall_s=0.0)
     results.close()
     results.join_thread()
     os._exit(code)
+
+
+def sp_prefill_worker(rank, world, port, B, Hq, Hkv, N, D, causal, seed):
+    """Each rank holds its block of Q, K and V, all-gathers K and V over gloo
+    and attends its rows with the global row offset (oracle as the local
+    attention); every rank checks its rows against the oracle over the whole
+    sequence."""
+    _init(rank, world, port)
+    import oracle
+    from attention_forward_sm_gb300 import sp_decode, sp_prefill
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(B, Hq, N, D, generator=g).to(torch.bfloat16)
+    k = torch.randn(B, Hkv, N, D, generator=g).to(torch.bfloat16)
+    v = torch.randn(B, Hkv, N, D, generator=g).to(torch.bfloat16)
+    scale = 1.0 / math.sqrt(D)
+    s0, s1 = sp_decode.shard_range(N, world, rank)
+    qb, kb, vb = (t[:, :, s0:s1].contiguous() for t in (q, k, v))
+
+    def local_attn(q_blk, k_full, v_full, causal_, q0, scale_):
+        # the oracle has no row offset: put the block behind q0 zero rows
+        n = q_blk.shape[2]
+        qpad = torch.cat([torch.zeros(B, Hq, q0, D, dtype=q_blk.dtype), q_blk], dim=2)
+        rows = [(b * Hq + h) * (q0 + n) + q0 + i for b in range(B) for h in range(Hq)
+                for i in range(n)]
+        o, l = oracle.attn_rows(qpad, k_full, v_full, B, Hq, Hkv, q0 + n, N, D, causal_,
+                                scale_, rows=rows)
+        return torch.from_numpy(o).reshape(B, Hq, n, D), torch.from_numpy(l).reshape(B, Hq, n)
+
+    o, lse = sp_prefill.sp_prefill(qb, kb, vb, N, causal, scale, local_attn=local_attn)
+    assert o.shape == (B, Hq, s1 - s0, D)
+    rows = [(b * Hq + h) * N + i for b in range(B) for h in range(Hq) for i in range(s0, s1)]
+    if rows:
+        o_ref, lse_ref = oracle.attn_rows(q, k, v, B, Hq, Hkv, N, N, D, causal, scale, rows=rows)
+        assert np.abs(o.reshape(-1, D).numpy() - o_ref).max() < 1e-12
+        assert np.abs(lse.reshape(-1).numpy() - lse_ref).max() < 1e-12
+    dist.destroy_process_group()

@@ -64,6 +64,18 @@ def test_fwd_validation(lib, args, status):
     assert lib.attn_fwd(*args, None) == status
 
 
+@pytest.mark.parametrize("q_offset,causal,status", [
+    (-1, 1, -3),                 # negative offset
+    (-1, 0, -3),                 # rejected without the causal mask too
+    (2**31 - 8 - 1024, 1, -3),   # offset + rows would overflow the kernel's int rows
+])
+def test_fwd_rows_validation(lib, q_offset, causal, status):
+    args = (ALIGNED,) * 5 + (1, 2, 2, 8, 8, 64, causal, q_offset, 0.1)
+    assert lib.attn_fwd_rows(*args, None) == status
+    bad_ptr = (0,) + (ALIGNED,) * 4 + (1, 2, 2, 8, 8, 64, causal, 0, 0.1)
+    assert lib.attn_fwd_rows(*bad_ptr, None) == -1
+
+
 @pytest.mark.parametrize("fn", ["attn_decode_splitkv", "attn_decode_splitkv_noalloc"])
 @pytest.mark.parametrize("args,status", [
     ((ALIGNED, 0, ALIGNED, ALIGNED, ALIGNED, 1, 4, 2, 16, 128, 4), -1),

@@ -47,6 +47,17 @@ def test_sp_flash_decode_gloo(world, Nk):
              nprocs=world, join=True)
 
 
+@pytest.mark.parametrize("world,N,causal", [(2, 300, True), (3, 200, True), (3, 130, False),
+                                            (4, 3, True)])
+def test_sp_prefill_gloo(world, N, causal):
+    """Sequence-parallel prefill on gloo ranks: K/V blocks all-gathered (ranks'
+    blocks differ in length; N = 3 on 4 ranks leaves one rank empty), each
+    rank's rows attended with their global offset, equal to the oracle over
+    the whole sequence."""
+    mp.spawn(W.sp_prefill_worker, args=(world, _free_port(), 1, 4, 2, N, 16, causal, 40 + world),
+             nprocs=world, join=True)
+
+
 @pytest.mark.parametrize("world,fail_rank,stall_s", [(2, 1, 0.0), (3, 0, 0.0), (3, 2, 0.0),
                                                      (2, 0, 12.0)])
 def test_sp_decode_rank_failure_is_detected(world, fail_rank, stall_s):
