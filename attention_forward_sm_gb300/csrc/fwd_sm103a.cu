@@ -1,5 +1,8 @@
 // Attention forward (prefill) for sm_103a: tiled, IO-aware, online softmax,
-// per-row log-sum-exp, causal mask and grouped KV heads.
+// per-row log-sum-exp, causal mask and grouped KV heads.  The causal mask can
+// sit at a global row offset (p.q_offset: row i of the launch is row
+// q_offset + i of the sequence), for a rank's block of a sequence-parallel
+// prefill.
 //
 // Method.  FlashAttention computes softmax(scale * Q K^T) V tile by tile
 // without writing the N x N score matrix to HBM ("FlashAttention-3 vs Triton
