@@ -12,6 +12,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "../../include/attn.h"
@@ -29,13 +30,15 @@ static __device__ __align__(256) float g_decode_scratch[kScratchFloats];
 
 constexpr int kMaxDevices = 64;
 
-// Per-device set-up, done once with that device current: check the compute
+// Per-device set-up, done with that device current: check the compute
 // capability and translate the scratch symbol into a device address (host
-// code cannot pass the symbol itself to a kernel).
+// code cannot pass the symbol itself to a kernel).  Under lazy module
+// loading the address lookup is also what loads the array onto the device,
+// so it can fail for lack of memory; only a completed set-up is kept, and a
+// failed one is tried again on the next call.
 struct ScratchState {
-  std::once_flag once;
-  cudaError_t err = cudaSuccess;
-  bool sm103 = false;
+  std::mutex mu;
+  std::atomic<int> ready{0};  // 1: sm_103, ptr valid; 2: not sm_103
   float* ptr = nullptr;
 };
 ScratchState g_state[kMaxDevices];
@@ -45,17 +48,32 @@ int scratch_for_current_device(float** out) {
   if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_DEVICE;
   ScratchState& st = g_state[dev];
-  std::call_once(st.once, [&st, dev] {
-    int major = 0, minor = 0;
-    st.err = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-    if (st.err == cudaSuccess)
-      st.err = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-    st.sm103 = (major == 10 && minor == 3);
-    if (st.err == cudaSuccess && st.sm103)
-      st.err = cudaGetSymbolAddress(reinterpret_cast<void**>(&st.ptr), g_decode_scratch);
-  });
-  if (st.err != cudaSuccess || (st.sm103 && st.ptr == nullptr)) return ATTN_ERR_CUDA;
-  if (!st.sm103) return ATTN_ERR_DEVICE;
+  int ready = st.ready.load(std::memory_order_acquire);
+  if (ready == 0) {
+    std::lock_guard<std::mutex> lock(st.mu);
+    ready = st.ready.load(std::memory_order_relaxed);
+    if (ready == 0) {
+      int major = 0, minor = 0;
+      if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+      if (major == 10 && minor == 3) {
+        float* ptr = nullptr;
+        if (cudaGetSymbolAddress(reinterpret_cast<void**>(&ptr), g_decode_scratch) !=
+                cudaSuccess ||
+            ptr == nullptr) {
+          cudaGetLastError();  // clear the (non-sticky) error so later calls do not see it
+          return ATTN_ERR_CUDA;
+        }
+        st.ptr = ptr;
+        ready = 1;
+      } else {
+        ready = 2;
+      }
+      st.ready.store(ready, std::memory_order_release);
+    }
+  }
+  if (ready == 2) return ATTN_ERR_DEVICE;
   *out = st.ptr;
   return ATTN_OK;
 }

@@ -242,8 +242,11 @@ int attn_combine_states(const float *part_o, const float *part_lse, void *o, flo
  * partial states live in a fixed array in device memory defined by this
  * library instead of in stream-ordered allocations.
  *
- *   - The array holds ATTN_NOALLOC_SCRATCH_BYTES on every device that loads
- *     the library, from load until the process exits.
+ *   - The array holds ATTN_NOALLOC_SCRATCH_BYTES of device memory on every
+ *     device where the library's code is loaded, until the process exits.
+ *     Under CUDA's default lazy module loading that happens during the
+ *     first call on each device, so that first call itself commits the
+ *     8 MiB: make it before reserving the rest of the device's memory.
  *   - A call needs B*Hq*nsplit*(D+1)*4 bytes of it (the decode workload
  *     B8 Hq32 D128 nsplit32 needs 4.2 MB); a larger problem returns
  *     ATTN_ERR_SCRATCH and launches nothing.
@@ -253,8 +256,10 @@ int attn_combine_states(const float *part_o, const float *part_lse, void *o, flo
  *     on the GPU -- e.g. on different streams without ordering between them
  *     -- race on the array and may both return wrong results: order them.
  *   - The first call on each device does a one-time set-up on the host (it
- *     looks up the array's device address for the current device); make
- *     that first call before any stream capture on that device.
+ *     loads the array and looks up its device address for the current
+ *     device); make that first call before any stream capture on that
+ *     device.  If the set-up fails (ATTN_ERR_CUDA, e.g. no memory left for
+ *     the array) nothing is cached and the next call tries again.
  *   - Calls nothing that allocates or frees memory.
  */
 int attn_decode_splitkv_noalloc(const void *q, const void *kcache, const void *vcache, void *o,

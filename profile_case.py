@@ -1,6 +1,6 @@
 """Run one library kernel on a small named case, for profilers (ncu).
 
-    python -m attention_forward_sm_gb300.profile_case fwd|fwd-causal|fwd-fp8|decode [--iters N]
+    python profile_case.py fwd|fwd-causal|fwd-d64|fwd-fp8|decode [--iters N]
 
 Each case keeps every input tensor above the 129 MB L2 but the whole case
 under ~1 GB of device memory, so a multi-pass ncu capture of one launch
@@ -11,16 +11,22 @@ bench.py.
 from __future__ import annotations
 
 import argparse
+import os
+import sys
 
 import torch
 
-from . import binding as attn
-from . import workloads as W
+sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+
+from attention_forward_sm_gb300 import binding as attn  # noqa: E402
+from attention_forward_sm_gb300 import workloads as W  # noqa: E402
 
 CASES = {
     # prefill: 4 x 32 heads x 4096 rows x 128: 134 MB per tensor
     "fwd": W.custom(4, 32, 32, 4096, 4096, 128, False, seed_index=900),
     "fwd-causal": W.custom(4, 32, 32, 4096, 4096, 128, True, seed_index=901),
+    # D = 64 prefill: 8 x 32 heads x 4096 rows x 64: 134 MB per tensor
+    "fwd-d64": W.custom(8, 32, 32, 4096, 4096, 64, False, seed_index=904),
     # decode: 8 x 8 KV heads x 16384 keys x 128: 268 MB per cache
     "decode": W.custom(8, 32, 8, 1, 16384, 128, False, seed_index=902, decode=True, nsplit=32),
     # FP8 prefill: the fwd shape with E4M3 inputs (67 MB per tensor, 134 MB for O)
