@@ -46,8 +46,10 @@ def run_fp8(w, q8, k8, vt8):
     return o, lse
 
 
-def check_fp8(w, o, lse, q8, k8, v8, rows=None, label=""):
-    args = (w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.D, w.causal, w.scale, SC["q"], SC["k"], SC["v"])
+def check_fp8(w, o, lse, q8, k8, v8, rows=None, label="", scales=None, scale=None):
+    sc = SC if scales is None else scales
+    args = (w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.D, w.causal, w.scale if scale is None else scale,
+            sc["q"], sc["k"], sc["v"])
     q8c, k8c, v8c = q8.cpu(), k8.cpu(), v8.cpu()
     o_ref, lse_ref = oracle.attn_rows_fp8(q8c, k8c, v8c, *args, rows=rows)
     # sum_j w_j |V_jd| * v_scale: the oracle on |V| (sign bit cleared)
@@ -60,7 +62,7 @@ def check_fp8(w, o, lse, q8, k8, v8, rows=None, label=""):
         og, lg = og[idx], lg[idx]
     assert np.isfinite(og).all() and np.isfinite(lg).all(), f"{label}: non-finite output"
     err = np.abs(og - o_ref)
-    bound = 2.0 ** -4 * o_abs + 2.0 ** -8 * np.abs(o_ref) + 2.0 ** -7 * SC["v"]
+    bound = 2.0 ** -4 * o_abs + 2.0 ** -8 * np.abs(o_ref) + 2.0 ** -7 * sc["v"]
     bad = err > bound
     assert not bad.any(), (f"{label}: {int(bad.sum())} elements out of tolerance, "
                            f"max |dO| = {err.max():.3e}, max |dO|/bound = {(err / bound).max():.3f}")
@@ -116,3 +118,56 @@ def test_fp8_argument_errors():
         attn.attn_fwd_fp8(q, q, q, o, lse, 1, 1, 1, 128, 128, 128, False, 0.1, 1, -1, 1)
     assert e.value.status == -3
     assert torch.count_nonzero(o).item() == 0
+
+
+# ----------------------------------------------------------------------------- correction path
+#
+# FP8 inputs that make the running max rise past its threshold (2 in log2
+# units) on most (row, tile) pairs, built and replayed on the host by
+# tests/correction_cases.py.  "exact": integer log2 scores with rises of
+# exactly 2 (no rescale: the weight reaches the 2^8 ceiling), 3 and 20, so
+# every weight is a power of two, exact in E4M3, and the output meets a
+# bound 16 times tighter than the general FP8 one -- a weight that
+# saturated at 448 (it would be 2^9 with the threshold one too high) fails
+# it; "near": rises 1.75 and 2.25; "ramp": N(0,1) inputs plus a key ramp.
+
+import correction_cases as CC  # noqa: E402
+
+FP8_CORRECTION_SHAPES = [
+    # B, Hq, Hkv, Nq, Nk, causal
+    (2, 4, 2, 300, 2000, False),
+    (1, 4, 1, 1008, 1008, True),   # FP8 keys: a multiple of 16
+]
+
+
+@pytest.mark.parametrize("construction", ["exact", "near", "ramp"])
+@pytest.mark.parametrize("shape", FP8_CORRECTION_SHAPES, ids=lambda s: "B{}Hq{}Hkv{}Nq{}Nk{}{}".format(
+    *s[:5], "c" if s[5] else ""))
+def test_fp8_correction_path(shape, construction):
+    B, Hq, Hkv, Nq, Nk, causal = shape
+    D = 128
+    full = (B, Hq, Hkv, Nq, Nk, D, causal)
+    case = CC.make_case(construction, "fp8", full)
+    u = CC.log2_scores(case, *full[:6])
+    fires, active, top = CC.replay_rescale(u, Nq, Nk, causal, case["R"])
+    frac = CC.fire_fraction(fires, active)
+    assert frac >= 0.5, f"the inputs rescale only {frac:.2f} of (row, tile >= 1) pairs"
+    sc = {"q": case["q_scale"], "k": case["k_scale"], "v": case["v_scale"]}
+    w = W.custom(B, Hq, Hkv, Nq, Nk, D, causal)
+    q8, k8, v8, vt8 = (case[x].cuda() for x in ("q8", "k8", "v8", "vt8"))
+    o = torch.empty((B, Hq, Nq, D), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device="cuda")
+    attn.attn_fwd_fp8(q8, k8, vt8, o, lse, B, Hq, Hkv, Nq, Nk, D, causal, case["scale"],
+                      sc["q"], sc["k"], sc["v"])
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_error() == 0
+    label = f"{construction} {shape} rescale on {frac:.2f}"
+    check_fp8(w, o, lse, q8, k8, v8, label=label, scales=sc, scale=case["scale"])
+    if construction == "exact":
+        assert top.max() == case["R"]   # some weight reaches 2^(2 + 6) = 2^8
+        o_ref, _ = oracle.attn_rows_fp8(q8.cpu(), k8.cpu(), v8.cpu(), B, Hq, Hkv, Nq, Nk, D,
+                                        causal, case["scale"], sc["q"], sc["k"], sc["v"])
+        og = o.float().cpu().numpy().astype(np.float64).reshape(-1, D)
+        bound = 2.0 ** -8 * np.abs(o_ref) + 2.0 ** -12 * sc["v"] * v8.float().abs().max().item()
+        bad = np.abs(og - o_ref) > bound
+        assert not bad.any(), f"{label}: {int(bad.sum())} elements over the tight bound"

@@ -321,3 +321,56 @@ def test_errors_are_returned_not_launched():
     assert e.value.status == -3
     assert torch.count_nonzero(o).item() == 0
     assert attn.attn_get_device_error() == 0
+
+
+# ----------------------------------------------------------------------------- correction path
+#
+# Inputs whose tile maxima climb, so the kernel's O rescale (the correction
+# step: the running max moved by more than 2^8) runs on most (row, tile)
+# pairs; tests/correction_cases.py builds them and replays the kernel's rule
+# on the host to show that it does.  "exact": integer log2 scores, rises of
+# exactly the threshold (no rescale), one over it and far over it, so every
+# weight is a power of two and the output also meets a tight bound;
+# "near": rises a quarter log2 unit under and over the threshold; "ramp":
+# N(0,1) inputs plus a key ramp.
+
+import correction_cases as CC  # noqa: E402
+
+CORRECTION_SHAPES = [
+    # B, Hq, Hkv, Nq, Nk, D, causal
+    (2, 4, 2, 300, 2000, 128, False),
+    (1, 4, 1, 1000, 1000, 128, True),
+    (2, 4, 2, 300, 2000, 64, False),
+    (1, 2, 2, 700, 1500, 64, True),
+]
+
+
+@pytest.mark.parametrize("construction", ["exact", "near", "ramp"])
+@pytest.mark.parametrize("shape", CORRECTION_SHAPES, ids=lambda s: "B{}Hq{}Hkv{}Nq{}Nk{}D{}{}".format(
+    *s[:6], "c" if s[6] else ""))
+def test_correction_path(shape, construction):
+    B, Hq, Hkv, Nq, Nk, D, causal = shape
+    case = CC.make_case(construction, "bf16", shape)
+    u = CC.log2_scores(case, B, Hq, Hkv, Nq, Nk, D)
+    fires, active, top = CC.replay_rescale(u, Nq, Nk, causal, case["R"])
+    frac = CC.fire_fraction(fires, active)
+    assert frac >= 0.5, f"the inputs rescale only {frac:.2f} of (row, tile >= 1) pairs"
+    w = W.custom(B, Hq, Hkv, Nq, Nk, D, causal)
+    q, k, v = (case[x].cuda() for x in "qkv")
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device="cuda")
+    attn.attn_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, causal, case["scale"])
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_error() == 0
+    o_ref, lse_ref = oracle_prefill(w, q, k, v, scale=case["scale"])
+    label = f"{construction} {shape} rescale on {frac:.2f}"
+    check(o, lse, o_ref.reshape(o.shape), lse_ref.reshape(lse.shape), label)
+    if construction == "exact":
+        # every weight is a power of two (the largest 2^8): the only rounding
+        # left is bf16 O (2^-9 relative) and fp32 accumulation
+        assert top.max() == case["R"]
+        og = o.float().cpu().numpy().astype(np.float64).reshape(-1, D)
+        ref = o_ref.reshape(-1, D)
+        bound = 2.0 ** -8 * np.abs(ref) + 1e-4 * v.float().abs().max().item()
+        bad = np.abs(og - ref) > bound
+        assert not bad.any(), f"{label}: {int(bad.sum())} elements over the tight bound"
