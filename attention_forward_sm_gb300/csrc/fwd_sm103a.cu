@@ -618,3 +618,15 @@ cudaError_t launch_fwd(const FwdParams& p, cudaStream_t stream) {
 }
 
 }  // namespace attn
+
+#ifdef ATTN_TRACE
+// Trace builds only: copies the event stamps of the last traced launch to
+// host memory (n words at most); returns the number copied or -1.
+extern "C" int attn_trace_copy(unsigned long long* host, int n) {
+  n = n < attn::kTraceCtas * 1024 ? n : attn::kTraceCtas * 1024;
+  return cudaMemcpyFromSymbol(host, attn::g_attn_trace, n * sizeof(unsigned long long)) ==
+                 cudaSuccess
+             ? n
+             : -1;
+}
+#endif
