@@ -119,7 +119,7 @@ __global__ void selftest_wait_kernel(unsigned int* err, uint64_t limit_ns) {
     fence_mbar_init();
   }
   __syncthreads();
-  mbar_wait(&bar, 0, &abort_flag, err, kErrSelfTest, limit_ns);
+  mbar_wait(&bar, 0, smem_u32(&abort_flag), err, kErrSelfTest, limit_ns);
 }
 
 }  // namespace
@@ -216,7 +216,8 @@ int attn_fwd_rows(const void* q, const void* k, const void* v, void* o, float* l
   // the kernel forms q_offset + (row within the call) + a few tiles in int
   if (q_offset < 0 || q_offset > INT_MAX - Nq - 1024) return ATTN_ERR_SHAPE;
   const long long nqb = (Nq + 255) / 256;
-  if (static_cast<long long>(B) * Hq * nqb >= (1ll << 31)) return ATTN_ERR_SHAPE;
+  // work units (pairs of query tiles) are counted in int, with a grid's worth of headroom
+  if (static_cast<long long>(B) * Hq * nqb >= (1ll << 31) - 65536) return ATTN_ERR_SHAPE;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return ATTN_ERR_ALIGN;
   DeviceState* st = nullptr;
@@ -226,7 +227,7 @@ int attn_fwd_rows(const void* q, const void* k, const void* v, void* o, float* l
   if (int rc = encode_3d(&p.tmap_q, q, D, Nq, static_cast<long long>(B) * Hq)) return rc;
   if (int rc = encode_3d(&p.tmap_k, k, D, Nk, static_cast<long long>(B) * Hkv)) return rc;
   if (int rc = encode_3d(&p.tmap_v, v, D, Nk, static_cast<long long>(B) * Hkv)) return rc;
-  if (int rc = encode_3d(&p.tmap_o, o, D, Nq, static_cast<long long>(B) * Hq)) return rc;
+  p.o = o;
   p.lse = lse;
   p.B = B;
   p.Hq = Hq;
@@ -255,7 +256,8 @@ int attn_fwd_fp8(const void* q, const void* k, const void* vt, void* o, float* l
   const float s_qk = scale * q_scale * k_scale;
   if (!isfinite(s_qk)) return ATTN_ERR_SHAPE;
   const long long nqb = (Nq + 255) / 256;
-  if (static_cast<long long>(B) * Hq * nqb >= (1ll << 31)) return ATTN_ERR_SHAPE;
+  // work units (pairs of query tiles) are counted in int, with a grid's worth of headroom
+  if (static_cast<long long>(B) * Hq * nqb >= (1ll << 31) - 65536) return ATTN_ERR_SHAPE;
   if (!aligned16(q) || !aligned16(k) || !aligned16(vt) || !aligned16(o) || !aligned16(lse))
     return ATTN_ERR_ALIGN;
   DeviceState* st = nullptr;
@@ -265,7 +267,7 @@ int attn_fwd_fp8(const void* q, const void* k, const void* vt, void* o, float* l
   if (int rc = encode_3d_e4m3(&p.tmap_q, q, D, Nq, static_cast<long long>(B) * Hq)) return rc;
   if (int rc = encode_3d_e4m3(&p.tmap_k, k, D, Nk, static_cast<long long>(B) * Hkv)) return rc;
   if (int rc = encode_3d_e4m3(&p.tmap_v, vt, Nk, D, static_cast<long long>(B) * Hkv)) return rc;
-  if (int rc = encode_3d(&p.tmap_o, o, D, Nq, static_cast<long long>(B) * Hq)) return rc;
+  p.o = o;
   p.lse = lse;
   p.B = B;
   p.Hq = Hq;

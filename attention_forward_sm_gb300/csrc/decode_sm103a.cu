@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(kDecThreads + 32, (GT >= 8 ? 1 : 2))
     fence_mbar_init();
   }
   __syncthreads();
-  volatile int* abort_p = &abort_flag;
+  const uint32_t abort_p = smem_u32(&abort_flag);
 
   if (warp == kDecWarps) {
     // ---------------------------------------------------------------- producer
@@ -214,7 +214,7 @@ __global__ void __launch_bounds__(kDecThreads + 32, (GT >= 8 ? 1 : 2))
                   &full_bar[slot], pol);
         issued = i + 1;
       }
-      if (*abort_p) {  // let the copies still in flight land before the CTA exits
+      if (abort_set(abort_p)) {  // let the copies still in flight land before the CTA exits
         for (int i = max(0, issued - kStages); i < issued; ++i)
           for (int spin = 0; spin < (1 << 20); ++spin)
             if (mbar_try_wait(&full_bar[i % kStages], (i / kStages) & 1)) break;

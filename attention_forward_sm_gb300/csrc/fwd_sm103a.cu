@@ -32,9 +32,11 @@
 //     exp2, row sum in fp32, P packed to bf16 into TMEM.  The same warps
 //     rescale O in TMEM, only when some row's max rose by more than 2^8
 //     (otherwise the stale max stays: exact, because the final division uses
-//     the same max), and run the epilogue (O / l -> bf16 -> swizzled smem ->
-//     TMA store, and LSE);
-//   * setmaxnreg moves registers from the load/MMA warps to the softmax warps.
+//     the same max), and run the epilogue (O / l -> bf16 -> global, and LSE);
+//   * setmaxnreg moves registers from the load/MMA warps to the softmax warps;
+//   * a CTA may work through several units in turn (non-causal: one CTA per
+//     SM), its TMEM, barriers and K/V ring carrying over, so the next unit's
+//     loads and first Q K^T overlap the current unit's tail.
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
@@ -63,8 +65,6 @@ struct Cfg {
   static constexpr int kAtomElems = 128 / kElemBytes;      // elements per 128-byte swizzle row
   static constexpr int kChunks = D * kElemBytes / 128;     // 128-byte swizzle chunks per tile row
   static constexpr int kStages = (D == 128) ? 4 : 8;       // K/V ring depth
-  static constexpr int kOutTileBytes = kBM * D * 2;        // a bf16 O tile
-  static constexpr int kOutChunks = D / 64;
   static constexpr int kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
   static constexpr int kTmemCols = 512;
   // P = 2^(s - m + kPBias) and the running max moves when it rises by more
@@ -74,31 +74,26 @@ struct Cfg {
   // weights out of the subnormal range (normal E4M3 starts at 2^-6).
   static constexpr float kPBias = kFp8 ? 6.f : 0.f;
   static constexpr float kRescale = kFp8 ? 2.f : 8.f;
-  // shared memory map (offsets from a 1024-byte aligned base).  O is staged
-  // for the TMA store in the tile's Q buffer when that holds a bf16 tile,
-  // else in a buffer of its own.
+  // dynamic shared memory map (offsets from a 1024-byte aligned base): the
+  // two Q tiles, the K/V ring (barriers are static shared memory)
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = 2 * kTileBytes;
-  static constexpr int kOffStage = kFp8 ? kOffKV + kStages * kTileBytes : kOffQ;
-  static constexpr int kOffMisc =
-      kFp8 ? kOffStage + 2 * kOutTileBytes : kOffKV + kStages * kTileBytes;
-  static constexpr int kMiscBytes = 4096;
-  static constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;  // + alignment slack
+  static constexpr int kSmemBytes = kOffKV + kStages * kTileBytes + 1024;  // + alignment slack
   static_assert(!kFp8 || D == kBN, "the FP8 V^T tile is D x 128 keys: D must be 128");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 
 struct Misc {
-  uint64_t q_full;
+  uint64_t q_full;        // the unit's Q tiles arrived (one phase per unit)
+  uint64_t q_empty;       // the unit's last Q K^T retired: Q buffers reusable
   uint64_t s_full[2];     // S_t = Q_t K^T in TMEM (MMA commit)
   uint64_t p_full[2];     // P_t in TMEM (one arrival per softmax warp of the tile)
-  uint64_t o_done[2];     // every MMA of O_t retired (single phase)
+  uint64_t o_done[2];     // every MMA of the unit's O_t retired (one phase per unit)
   uint64_t mma_done;
   uint64_t kv_full[8], kv_empty[8];
   uint32_t tmem_base;
   int abort_flag;
 };
-static_assert(sizeof(Misc) <= 4096, "misc region");
 
 __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xFFFFFFFFu, v); }
 
@@ -126,55 +121,83 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return;
 }
 
-// S = Q K^T over the head dimension, one MMA per 32 bytes of a row (16 bf16
-// or 32 e4m3 columns); inside a 128-byte swizzle chunk a k-step advances the
-// start address by 32 bytes, the next chunk starts 128 rows * 128 bytes
-// further.
-template <bool kFp8, int KK, int NK>
-__device__ __forceinline__ void issue_s_rec(uint32_t d, uint64_t a0, uint64_t b0, uint32_t idesc) {
+// S = Q K^T over the head dimension into TMEM columns kColD, one MMA per 32
+// bytes of a row (16 bf16 or 32 e4m3 columns); inside a 128-byte swizzle
+// chunk a k-step advances the start address by 32 bytes, the next chunk
+// starts 128 rows * 128 bytes further.
+template <bool kFp8, uint32_t kColD, int KK, int NK>
+__device__ __forceinline__ void issue_s_rec(uint32_t tmem, uint32_t a0, uint32_t b0,
+                                            uint32_t idesc) {
   if constexpr (KK < NK) {
     constexpr uint32_t off = ((KK >> 2) * (kBM * 128) + (KK & 3) * 32) >> 4;
-    if constexpr (kFp8)
-      mma_ss_off_f8<off, off>(d, a0, b0, idesc, KK > 0 ? 1u : 0u);
-    else
-      mma_ss_off<off, off>(d, a0, b0, idesc, KK > 0 ? 1u : 0u);
-    issue_s_rec<kFp8, KK + 1, NK>(d, a0, b0, idesc);
+    mma_ss<kFp8, kColD, off, off>(tmem, a0, b0, idesc, KK > 0 ? 1u : 0u);
+    issue_s_rec<kFp8, kColD, KK + 1, NK>(tmem, a0, b0, idesc);
   }
 }
-template <int D, bool kFp8>
-__device__ __forceinline__ void issue_s_steps(uint32_t d, uint64_t a0, uint64_t b0,
+template <int D, bool kFp8, uint32_t kColD>
+__device__ __forceinline__ void issue_s_steps(uint32_t tmem, uint32_t a0, uint32_t b0,
                                               uint32_t idesc) {
-  issue_s_rec<kFp8, 0, D * (kFp8 ? 1 : 2) / 32>(d, a0, b0, idesc);
+  issue_s_rec<kFp8, kColD, 0, D * (kFp8 ? 1 : 2) / 32>(tmem, a0, b0, idesc);
 }
-// O += P V over the 128 keys of a tile, one MMA per 8 TMEM columns of P
-// (16 bf16 or 32 e4m3 keys).  bf16: V is MN-major, a step advances 16 rows
-// * 128 bytes.  e4m3: V^T (D rows of 128 keys) is K-major, a step advances
-// 32 bytes inside the 128-byte row.
-template <bool kFp8, int KK>
-__device__ __forceinline__ void issue_pv_rec(uint32_t d, uint32_t a, uint64_t b0, uint32_t idesc,
+// O (TMEM columns kColD) += P (TMEM columns kColP) V over the 128 keys of a
+// tile, one MMA per 8 TMEM columns of P (16 bf16 or 32 e4m3 keys).  bf16: V
+// is MN-major, a step advances 16 rows * 128 bytes.  e4m3: V^T (D rows of
+// 128 keys) is K-major, a step advances 32 bytes inside the 128-byte row.
+template <bool kFp8, uint32_t kColD, uint32_t kColP, int KK>
+__device__ __forceinline__ void issue_pv_rec(uint32_t tmem, uint32_t b0, uint32_t idesc,
                                              uint32_t acc) {
   constexpr int kSteps = kFp8 ? kBN / 32 : kBN / 16;
   if constexpr (KK < kSteps) {
-    if constexpr (kFp8)
-      mma_ts_off_f8<((KK * 32) >> 4)>(d, a + KK * 8, b0, idesc, (acc | KK) ? 1u : 0u);
-    else
-      mma_ts_off<((KK * 16 * 128) >> 4)>(d, a + KK * 8, b0, idesc, (acc | KK) ? 1u : 0u);
-    issue_pv_rec<kFp8, KK + 1>(d, a, b0, idesc, acc);
+    constexpr uint32_t off = kFp8 ? ((KK * 32) >> 4) : ((KK * 16 * 128) >> 4);
+    mma_ts<kFp8, kColD, kColP + KK * 8, off>(tmem, b0, idesc, KK > 0 ? 1u : acc);
+    issue_pv_rec<kFp8, kColD, kColP, KK + 1>(tmem, b0, idesc, acc);
   }
 }
-template <bool kFp8>
-__device__ __forceinline__ void issue_pv_steps(uint32_t d, uint32_t a, uint64_t b0, uint32_t idesc,
+template <bool kFp8, uint32_t kColD, uint32_t kColP>
+__device__ __forceinline__ void issue_pv_steps(uint32_t tmem, uint32_t b0, uint32_t idesc,
                                                uint32_t acc) {
-  issue_pv_rec<kFp8, 0>(d, a, b0, idesc, acc);
+  issue_pv_rec<kFp8, kColD, kColP, 0>(tmem, b0, idesc, acc);
 }
 
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-               "r"(d)
-               : "memory");
+// Work unit u: (batch*head, pair of 128-row query tiles).  Non-causal:
+// head-major.  Causal: heads in groups of p.group_heads (sized on the host
+// so a group's K/V stays in L2); inside a group all units longest first, so
+// the CTAs, which take units in order, end every group, and the grid, on
+// short units.
+struct Unit {
+  int bh, q_base, n_kv;
+};
+__device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u, int nqb) {
+  int qblk, bh;
+  if (p.causal) {
+    const int BH = p.B * p.Hq;
+    const int per_group = p.group_heads * nqb;
+    const int g = u / per_group;
+    const int idx = u % per_group;
+    const int heads = min(p.group_heads, BH - g * p.group_heads);
+    qblk = nqb - 1 - idx / heads;
+    bh = g * p.group_heads + idx % heads;
+  } else {
+    qblk = u % nqb;
+    bh = u / nqb;
+  }
+  Unit w;
+  w.bh = bh;
+  w.q_base = qblk * 2 * kBM;
+  w.n_kv = (p.Nk + kBN - 1) / kBN;
+  if (p.causal) w.n_kv = min(w.n_kv, (w.q_base + p.q_offset + 2 * kBM + kBN - 1) / kBN);
+  return w;
+}
+__device__ __forceinline__ int kv_head(const FwdParams& p, int bh) {
+  return (bh / p.Hq) * p.Hkv + (bh % p.Hq) / (p.Hq / p.Hkv);
 }
 
+// Each CTA works through units blockIdx.x, blockIdx.x + gridDim.x, ... (one
+// unit when the grid covers them all; a persistent grid of one CTA per SM
+// otherwise).  TMEM, barriers and the K/V ring live across units: every
+// barrier phase and the ring position run on, so the next unit's K/V and Q
+// loads and its first Q K^T overlap the current unit's last steps and
+// epilogue.
 template <int D, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ FwdParams p) {
@@ -182,38 +205,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  Misc& ms = *reinterpret_cast<Misc*>(smem + C::kOffMisc);
-  volatile int* abort_flag = &ms.abort_flag;
+  // barriers in static shared memory: their addresses are constants, which
+  // keeps them out of the registers of the 32-register warps
+  __shared__ Misc ms;
+  const uint32_t abort_flag = smem_u32(&ms.abort_flag);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  // ---- work unit: (batch*head, pair of 128-row query tiles).  Non-causal:
-  // head-major.  Causal: heads in groups of p.group_heads (sized on the host
-  // so a group's K/V stays in L2); inside a group all units longest first,
-  // so the block scheduler ends every group, and the grid, on short units.
-  const int nqb = (p.Nq + 2 * kBM - 1) / (2 * kBM);
-  int qblk, bh;
-  if (p.causal) {
-    const int BH = p.B * p.Hq;
-    const int per_group = p.group_heads * nqb;
-    const int g = static_cast<int>(blockIdx.x / per_group);
-    const int idx = static_cast<int>(blockIdx.x % per_group);
-    const int heads = min(p.group_heads, BH - g * p.group_heads);
-    qblk = nqb - 1 - idx / heads;
-    bh = g * p.group_heads + idx % heads;
-  } else {
-    qblk = static_cast<int>(blockIdx.x % nqb);
-    bh = static_cast<int>(blockIdx.x / nqb);
-  }
-  const int q_base = qblk * 2 * kBM;
-  const int G = p.Hq / p.Hkv;
-  const int bhkv = (bh / p.Hq) * p.Hkv + (bh % p.Hq) / G;
-  int n_kv = (p.Nk + kBN - 1) / kBN;
-  if (p.causal) n_kv = min(n_kv, (q_base + p.q_offset + 2 * kBM + kBN - 1) / kBN);
+  // (recomputed where used rather than kept live into the roles)
+#define ATTN_NQB ((p.Nq + 2 * kBM - 1) / (2 * kBM))
+#define ATTN_UNITS (ATTN_NQB * p.B * p.Hq)
 
   // ---- setup: barriers (loader warp), TMEM (MMA warp)
   if (warp == kWarpLoad && lane == 0) {
     mbar_init(&ms.q_full, 1);
+    mbar_init(&ms.q_empty, 1);
     for (int t = 0; t < 2; ++t) {
       mbar_init(&ms.s_full[t], 1);
       mbar_init(&ms.p_full[t], 8);
@@ -226,20 +231,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ms.abort_flag = 0;
     fence_mbar_init();
-    // The Q tiles and the first K tile start loading now, before the CTA-wide
-    // barrier and the TMEM allocation: they are the first MMA's operands.
+    // The first unit's Q tiles and first K tile start loading now, before the
+    // CTA-wide barrier and the TMEM allocation: they are the first MMA's
+    // operands.
+    const Unit w = decode_unit(p, static_cast<int>(blockIdx.x), ATTN_NQB);
     mbar_arrive_expect_tx(&ms.q_full, 2 * C::kTileBytes);
     for (int t = 0; t < 2; ++t)
       for (int ch = 0; ch < C::kChunks; ++ch)
         tma_load_3d(smem + C::kOffQ + t * C::kTileBytes + ch * (kBM * 128), &p.tmap_q,
-                    &ms.q_full, ch * C::kAtomElems, q_base + t * kBM, bh,
+                    &ms.q_full, ch * C::kAtomElems, w.q_base + t * kBM, w.bh,
                     l2_policy_evict_first());
     mbar_arrive_expect_tx(&ms.kv_full[0], C::kTileBytes);
     for (int ch = 0; ch < C::kChunks; ++ch)
       tma_load_3d(smem + C::kOffKV + ch * (kBM * 128), &p.tmap_k, &ms.kv_full[0],
-                  ch * C::kAtomElems, 0, bhkv, l2_policy_evict_last());
+                  ch * C::kAtomElems, 0, kv_head(p, w.bh), l2_policy_evict_last());
     tma_prefetch_desc(&p.tmap_v);
-    tma_prefetch_desc(&p.tmap_o);
   }
   if (warp == kWarpMma) {
     tmem_alloc(&ms.tmem_base, C::kTmemCols);
@@ -249,7 +255,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ms.tmem_base;
-  const uint64_t lim = p.wait_limit_ns;
 
   if (warp < 16) {
     // =====================================================================
@@ -264,214 +269,244 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lbase = (warp & 3) * 32 + ((warp >> 2) & 1) * 16;  // first TMEM lane of the warp
     const int r = lbase + (lane & 15);                              // row within the tile
     const int c = lane >> 4;                                        // column half of the row
-    const int row = q_base + t * kBM + r;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(lbase) << 16);
     const uint32_t s_addr = lane_addr + (t ? C::kColS1 : C::kColS0);
     const uint32_t o_addr = lane_addr + (t ? C::kColO1 : C::kColO0);
-    const int tile_row0 = q_base + t * kBM;
-    const int vis = p.causal ? min(row + 1 + p.q_offset, p.Nk) : p.Nk;  // keys [0, vis) visible
     const bool tracer = (warp & 7) == 0 && lane == 0;
-    float m = -CUDART_INF_F, l = 0.f;  // l: sum over this thread's half of the row
+    uint32_t step = 0;  // key tiles of this CTA's earlier units: barrier phases run on
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      if (!warp_all(mbar_wait(&ms.s_full[t], j & 1, abort_flag, p.err, kErrWaitSoftmax, lim))) {
-        ok = false;
-        break;
-      }
-      if (tracer) ATTN_TRACE_EV(0, t, j);
-      tc_fence_after();
-      float s[64];
-      {
-        uint32_t sr[64];
-        tmem_ld_pair64<64>(s_addr, sr);
-#pragma unroll
-        for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(sr[i]);
-      }
-      if (tracer) ATTN_TRACE_EV(1, t, j);
-      const int kb = j * kBN + c * 64;  // key index of this thread's first column
-      const bool need_mask =
-          (j * kBN + kBN > p.Nk) || (p.causal && j * kBN + kBN - 1 > tile_row0 + p.q_offset);
-      if (need_mask) {
-        const int lim_c = vis - kb;  // columns [0, lim_c) valid
-#pragma unroll
-        for (int i = 0; i < 64; ++i)
-          if (i >= lim_c) s[i] = -CUDART_INF_F;
-      }
-      float mx;
-      {
-        float a0 = fmaxf(s[0], s[1]), a1 = fmaxf(s[2], s[3]);
-        float a2 = fmaxf(s[4], s[5]), a3 = fmaxf(s[6], s[7]);
-#pragma unroll
-        for (int i = 8; i < 64; i += 8) {
-          a0 = max3f(a0, s[i], s[i + 1]);
-          a1 = max3f(a1, s[i + 2], s[i + 3]);
-          a2 = max3f(a2, s[i + 4], s[i + 5]);
-          a3 = max3f(a3, s[i + 6], s[i + 7]);
+    for (int u = static_cast<int>(blockIdx.x), k = 0; u < ATTN_UNITS && ok;
+         u += static_cast<int>(gridDim.x), ++k) {
+      const Unit w = decode_unit(p, u, ATTN_NQB);
+      const int tile_row0 = w.q_base + t * kBM;
+      const int row = tile_row0 + r;
+      const int vis = p.causal ? min(row + 1 + p.q_offset, p.Nk) : p.Nk;  // keys [0, vis)
+      float m = -CUDART_INF_F, l = 0.f;  // l: sum over this thread's half of the row
+      for (int j = 0; j < w.n_kv; ++j) {
+        if (!warp_all(mbar_wait(&ms.s_full[t], (step + j) & 1, abort_flag, p.err,
+                                kErrWaitSoftmax, p.wait_limit_ns))) {
+          ok = false;
+          break;
         }
-        mx = max3f(a0, a1, fmaxf(a2, a3));
-        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));  // the row's other half
-      }
-      // running max in log2 units (scale >= 0, so max commutes with scaling)
-      const float m_tile = (mx == -CUDART_INF_F) ? -CUDART_INF_F : mx * p.scale_log2;
-      float alpha = 1.f;
-      if (m_tile > m + C::kRescale || m == -CUDART_INF_F) {
-        alpha = ex2_approx(m - m_tile);  // 0 on the first tile
-        m = m_tile;
-      }
-      if (tracer) ATTN_TRACE_EV(2, t, j);
-      // p = 2^(s*scale*log2e - m + bias), masked entries exactly 0; packed
-      // to bf16 pairs (32 words) or e4m3 quads (16 words), low key first
-      const float neg_m = C::kPBias - m;
-      float rsum;
-      uint32_t pk[kFp8 ? 16 : 32];
-      auto pack4 = [&](int i, float p0, float p1, float p2, float p3) {
-        if constexpr (kFp8) {
-          pk[i / 4] = pack_e4m3x4(p0, p1, p2, p3);
+        if (tracer && k == 0) ATTN_TRACE_EV(0, t, j);
+        tc_fence_after();
+        float s[64];
+        {
+          uint32_t sr[64];
+          tmem_ld_pair64<64>(s_addr, sr);
+#pragma unroll
+          for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(sr[i]);
+        }
+        if (tracer && k == 0) ATTN_TRACE_EV(1, t, j);
+        const int kb = j * kBN + c * 64;  // key index of this thread's first column
+        const bool need_mask =
+            (j * kBN + kBN > p.Nk) || (p.causal && j * kBN + kBN - 1 > tile_row0 + p.q_offset);
+        if (need_mask) {
+          const int lim_c = vis - kb;  // columns [0, lim_c) valid
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            if (i >= lim_c) s[i] = -CUDART_INF_F;
+        }
+        float mx;
+        {
+          float a0 = fmaxf(s[0], s[1]), a1 = fmaxf(s[2], s[3]);
+          float a2 = fmaxf(s[4], s[5]), a3 = fmaxf(s[6], s[7]);
+#pragma unroll
+          for (int i = 8; i < 64; i += 8) {
+            a0 = max3f(a0, s[i], s[i + 1]);
+            a1 = max3f(a1, s[i + 2], s[i + 3]);
+            a2 = max3f(a2, s[i + 4], s[i + 5]);
+            a3 = max3f(a3, s[i + 6], s[i + 7]);
+          }
+          mx = max3f(a0, a1, fmaxf(a2, a3));
+          mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));  // the row's other half
+        }
+        // running max in log2 units (scale >= 0, so max commutes with scaling)
+        const float m_tile = (mx == -CUDART_INF_F) ? -CUDART_INF_F : mx * p.scale_log2;
+        float alpha = 1.f;
+        if (m_tile > m + C::kRescale || m == -CUDART_INF_F) {
+          alpha = ex2_approx(m - m_tile);  // 0 on the first tile
+          m = m_tile;
+        }
+        if (tracer && k == 0) ATTN_TRACE_EV(2, t, j);
+        // p = 2^(s*scale*log2e - m + bias), masked entries exactly 0; packed
+        // to bf16 pairs (32 words) or e4m3 quads (16 words), low key first
+        const float neg_m = C::kPBias - m;
+        float rsum;
+        uint32_t pk[kFp8 ? 16 : 32];
+        auto pack4 = [&](int i, float p0, float p1, float p2, float p3) {
+          if constexpr (kFp8) {
+            pk[i / 4] = pack_e4m3x4(p0, p1, p2, p3);
+          } else {
+            pk[i / 2] = pack_bf16x2(p0, p1);
+            pk[i / 2 + 1] = pack_bf16x2(p2, p3);
+          }
+        };
+        if (need_mask) {
+          float r0 = 0.f, r1 = 0.f;
+#pragma unroll
+          for (int i = 0; i < 64; i += 4) {
+            float pp[4];
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              pp[v] = (s[i + v] == -CUDART_INF_F)
+                          ? 0.f
+                          : ex2_approx(fmaf(s[i + v], p.scale_log2, neg_m));
+            r0 += pp[0] + pp[2];
+            r1 += pp[1] + pp[3];
+            pack4(i, pp[0], pp[1], pp[2], pp[3]);
+          }
+          rsum = r0 + r1;
         } else {
-          pk[i / 2] = pack_bf16x2(p0, p1);
-          pk[i / 2 + 1] = pack_bf16x2(p2, p3);
+          // packed fp32x2: one FMA and one add per pair of columns
+          const uint64_t scale2 = f32x2(p.scale_log2, p.scale_log2);
+          const uint64_t negm2 = f32x2(neg_m, neg_m);
+          uint64_t acc0 = f32x2(0.f, 0.f), acc1 = acc0;
+#pragma unroll
+          for (int i = 0; i < 64; i += 4) {
+            float x0, x1, x2, x3;
+            unpack_f32x2(fma_f32x2(f32x2(s[i], s[i + 1]), scale2, negm2), x0, x1);
+            unpack_f32x2(fma_f32x2(f32x2(s[i + 2], s[i + 3]), scale2, negm2), x2, x3);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+            acc0 = add_f32x2(acc0, f32x2(p0, p1));
+            acc1 = add_f32x2(acc1, f32x2(p2, p3));
+            pack4(i, p0, p1, p2, p3);
+          }
+          float u0f, u1f;
+          unpack_f32x2(add_f32x2(acc0, acc1), u0f, u1f);
+          rsum = u0f + u1f;
         }
-      };
-      if (need_mask) {
-        float r0 = 0.f, r1 = 0.f;
+        l = fmaf(l, alpha, rsum);
+        if (tracer && k == 0) ATTN_TRACE_EV(3, t, j);
+        // Rescale O_t when a row's max rose past the threshold.  Every P*V of
+        // KV tiles < j has retired: it was issued before S_t(j), whose
+        // completion woke this warp.  The P*V of tile j waits for p_full below.
+        // Thread half c owns O columns [c*D/2, (c+1)*D/2) of its row.
+        if (j > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.f)) {
+          // 16 columns at a time: P (pk) stays live across this rare path
+#pragma unroll 1
+          for (int kk = 0; kk < D / 32; ++kk) {
+            uint32_t v[16];
+            tmem_ld_pair16<D / 2>(o_addr + kk * 16, v);
 #pragma unroll
-        for (int i = 0; i < 64; i += 4) {
-          float pp[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            pp[u] = (s[i + u] == -CUDART_INF_F) ? 0.f
-                                                : ex2_approx(fmaf(s[i + u], p.scale_log2, neg_m));
-          r0 += pp[0] + pp[2];
-          r1 += pp[1] + pp[3];
-          pack4(i, pp[0], pp[1], pp[2], pp[3]);
+            for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+            tmem_st_pair16<D / 2>(o_addr + kk * 16, v);
+          }
+          tmem_st_wait();
         }
-        rsum = r0 + r1;
-      } else {
-        // packed fp32x2: one FMA and one add per pair of columns
-        const uint64_t scale2 = f32x2(p.scale_log2, p.scale_log2);
-        const uint64_t negm2 = f32x2(neg_m, neg_m);
-        uint64_t acc0 = f32x2(0.f, 0.f), acc1 = acc0;
-#pragma unroll
-        for (int i = 0; i < 64; i += 4) {
-          float x0, x1, x2, x3;
-          unpack_f32x2(fma_f32x2(f32x2(s[i], s[i + 1]), scale2, negm2), x0, x1);
-          unpack_f32x2(fma_f32x2(f32x2(s[i + 2], s[i + 3]), scale2, negm2), x2, x3);
-          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-          const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
-          acc0 = add_f32x2(acc0, f32x2(p0, p1));
-          acc1 = add_f32x2(acc1, f32x2(p2, p3));
-          pack4(i, p0, p1, p2, p3);
-        }
-        float u0, u1;
-        unpack_f32x2(add_f32x2(acc0, acc1), u0, u1);
-        rsum = u0 + u1;
-      }
-      l = fmaf(l, alpha, rsum);
-      if (tracer) ATTN_TRACE_EV(3, t, j);
-      // Rescale O_t when a row's max rose past the threshold.  Every P*V of KV
-      // tiles < j has retired: it was issued before S_t(j), whose completion
-      // woke this warp.  The P*V of tile j waits for p_full below.  Thread half
-      // c owns O columns [c*D/2, (c+1)*D/2) of its row.
-      if (j > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.f)) {
-#pragma unroll
-        for (int k = 0; k < D / 64; ++k) {
-          uint32_t v[32];
-          tmem_ld_pair32<D / 2>(o_addr + k * 32, v);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-          tmem_st_pair32<D / 2>(o_addr + k * 32, v);
-        }
+        // P over the first 64 (bf16) or 32 (e4m3) columns of S: this half's
+        // 32 or 16 columns
+        if constexpr (kFp8)
+          tmem_st_pair16<16>(s_addr, pk);
+        else
+          tmem_st_pair32<32>(s_addr, pk);
         tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ms.p_full[t]);
+        if (tracer && k == 0) ATTN_TRACE_EV(4, t, j);
       }
-      // P over the first 64 (bf16) or 32 (e4m3) columns of S: this half's
-      // 32 or 16 columns
-      if constexpr (kFp8)
-        tmem_st_pair16<16>(s_addr, pk);
-      else
-        tmem_st_pair32<32>(s_addr, pk);
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ms.p_full[t]);
-      if (tracer) ATTN_TRACE_EV(4, t, j);
-    }
-    // ---- epilogue of tile t: O / l -> bf16 -> swizzled smem (the tile's Q
-    // buffer) -> TMA store; LSE.  Every warp of the tile reaches the named
-    // barrier exactly once, also after an abort.
-    const float l_row = l + __shfl_xor_sync(0xFFFFFFFFu, l, 16);
-    const bool good =
-        ok && warp_all(mbar_wait(&ms.o_done[t], 0, abort_flag, p.err, kErrWaitCorr, lim));
-    uint8_t* stage = smem + C::kOffStage + t * C::kOutTileBytes;
-    if (good) {
+      step += w.n_kv;
+      // ---- epilogue of tile t: O / l -> bf16 -> global (a thread writes the
+      // D/2 columns it owns of its row), and LSE.  The TMEM reads of O_t
+      // complete here, before these warps publish the next unit's first P of
+      // this tile, which the MMA that overwrites O_t waits for.
+      ok = ok && warp_all(mbar_wait(&ms.o_done[t], k & 1, abort_flag, p.err, kErrWaitCorr, p.wait_limit_ns));
+      if (!ok) break;
       tc_fence_after();
+      const float l_row = l + __shfl_xor_sync(0xFFFFFFFFu, l, 16);
       const float inv = p.o_scale / l_row;
-      const uint32_t stage_row = smem_u32(stage) + r * 128;
+      uint4* orow = reinterpret_cast<uint4*>(
+          static_cast<__nv_bfloat16*>(p.o) +
+          (static_cast<size_t>(w.bh) * p.Nq + static_cast<size_t>(row)) * D + c * (D / 2));
 #pragma unroll
-      for (int k = 0; k < D / 64; ++k) {
-        // columns c*D/2 + [32k, 32k + 32) of the row
+      for (int kk = 0; kk < D / 64; ++kk) {
+        // columns c*D/2 + [32kk, 32kk + 32) of the row
         uint32_t v[32];
-        tmem_ld_pair32<D / 2>(o_addr + k * 32, v);
-        uint32_t w[16];
+        tmem_ld_pair32<D / 2>(o_addr + kk * 32, v);
+        uint32_t wv[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-          w[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * inv, __uint_as_float(v[2 * i + 1]) * inv);
-        const int col0 = c * (D / 2) + 32 * k;  // first of the 32 columns
+          wv[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * inv,
+                              __uint_as_float(v[2 * i + 1]) * inv);
+        if (row < p.Nq) {
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const int col = col0 + 8 * g;               // 8 bf16 = one 16-byte granule
-          const int chunk = col >> 6, gran = (col & 63) >> 3;
-          const uint32_t addr = stage_row + chunk * (kBM * 128) + ((gran ^ (r & 7)) << 4);
-          st_shared_v4(addr, w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
+          for (int g = 0; g < 4; ++g)
+            orow[kk * 4 + g] = make_uint4(wv[4 * g], wv[4 * g + 1], wv[4 * g + 2], wv[4 * g + 3]);
         }
       }
       if (c == 0 && row < p.Nq)
-        p.lse[static_cast<size_t>(bh) * p.Nq + row] =
+        p.lse[static_cast<size_t>(w.bh) * p.Nq + row] =
             (m - C::kPBias + __log2f(l_row)) * 0.69314718055994530942f;
-    }
-    fence_proxy_async_smem();
-    named_bar_sync(1 + t, 256);
-    if ((warp & 7) == 0 && lane == 0) {
-      if (!*abort_flag && q_base + t * kBM < p.Nq) {
-#pragma unroll
-        for (int ch = 0; ch < C::kOutChunks; ++ch)
-          tma_store_3d(&p.tmap_o, stage + ch * (kBM * 128), ch * 64, q_base + t * kBM, bh);
-        tma_store_commit();
-      }
-      tma_store_wait_all0();
     }
   } else if (warp == kWarpLoad) {
     // =====================================================================
-    // TMA loader: Q tiles once, then K_j, V_j through the ring
+    // TMA loader: per unit the Q tiles (once the previous unit's last Q K^T
+    // has read them), then K_j, V_j through the ring.  Ring item numbers run
+    // on across units: a unit's step j loads items 2(step + j), +1.
     // =====================================================================
     reg_dealloc<kRegOther>();
     if (lane == 0) {
-      const uint64_t pol_kv = l2_policy_evict_last();
-      // Q and K_0 were issued during setup
-      int issued = 1;
-      for (int it = 1; it < 2 * n_kv; ++it) {
-        const int s = it % C::kStages;
-        const uint32_t ph = static_cast<uint32_t>(it / C::kStages) & 1u;
-        if (!mbar_wait(&ms.kv_empty[s], ph ^ 1u, abort_flag, p.err, kErrWaitLoad, lim)) break;
-        ATTN_TRACE_EV(7, it & 1, it >> 1);
-        mbar_arrive_expect_tx(&ms.kv_full[s], C::kTileBytes);
-        uint8_t* dst = smem + C::kOffKV + s * C::kTileBytes;
-        if (kFp8 && (it & 1)) {
-          // V^T [D rows, keys]: rows 0..D-1, keys of tile it/2
-          tma_load_3d(dst, &p.tmap_v, &ms.kv_full[s], (it >> 1) * kBN, 0, bhkv, pol_kv);
-        } else {
-          const CUtensorMap* map = (it & 1) ? &p.tmap_v : &p.tmap_k;
-          for (int ch = 0; ch < C::kChunks; ++ch)
-            tma_load_3d(dst + ch * (kBM * 128), map, &ms.kv_full[s], ch * C::kAtomElems,
-                        (it >> 1) * kBN, bhkv, pol_kv);
+      uint32_t item = 0;    // ring items of earlier units
+      uint32_t g = 1;       // next ring item (the first unit's K_0 was issued during setup)
+      uint32_t q_phase = 0;  // q_full phase of the last Q load issued
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int u = static_cast<int>(blockIdx.x + k * gridDim.x);
+        if (u >= ATTN_UNITS) break;
+        const Unit w = decode_unit(p, u, ATTN_NQB);
+        const int bhkv = kv_head(p, w.bh);
+        const uint32_t item_end = item + 2u * static_cast<uint32_t>(w.n_kv);
+        for (; g < item_end; ++g) {
+          const uint32_t it = g - item;  // item within the unit: K_{it/2} or V_{it/2}
+          const uint32_t s = g % C::kStages;
+          if (!mbar_wait(&ms.kv_empty[s], ((g / C::kStages) & 1u) ^ 1u, abort_flag, p.err,
+                         kErrWaitLoad, p.wait_limit_ns)) {
+            ok = false;
+            break;
+          }
+          if (k == 0) ATTN_TRACE_EV(7, it & 1, it >> 1);
+          mbar_arrive_expect_tx(&ms.kv_full[s], C::kTileBytes);
+          uint8_t* dst = smem + C::kOffKV + s * C::kTileBytes;
+          const int jt = static_cast<int>(it >> 1);
+          if (kFp8 && (it & 1)) {
+            // V^T [D rows, keys]: rows 0..D-1, keys of tile jt
+            tma_load_3d(dst, &p.tmap_v, &ms.kv_full[s], jt * kBN, 0, bhkv,
+                        l2_policy_evict_last());
+          } else {
+            const CUtensorMap* map = (it & 1) ? &p.tmap_v : &p.tmap_k;
+            for (int ch = 0; ch < C::kChunks; ++ch)
+              tma_load_3d(dst + ch * (kBM * 128), map, &ms.kv_full[s], ch * C::kAtomElems,
+                          jt * kBN, bhkv, l2_policy_evict_last());
+          }
+          if (it == 0 && k > 0) {
+            // the Q tiles of this unit, once the previous unit's last Q K^T
+            // retired (its K_0 is already on the way)
+            if (!mbar_wait(&ms.q_empty, (k - 1) & 1, abort_flag, p.err, kErrWaitLoad,
+                           p.wait_limit_ns)) {
+              ok = false;
+              ++g;
+              break;
+            }
+            const Unit wq = decode_unit(p, u, ATTN_NQB);
+            q_phase = k & 1;
+            mbar_arrive_expect_tx(&ms.q_full, 2 * C::kTileBytes);
+            for (int t = 0; t < 2; ++t)
+              for (int ch = 0; ch < C::kChunks; ++ch)
+                tma_load_3d(smem + C::kOffQ + t * C::kTileBytes + ch * (kBM * 128), &p.tmap_q,
+                            &ms.q_full, ch * C::kAtomElems, wq.q_base + t * kBM, wq.bh,
+                            l2_policy_evict_first());
+          }
         }
-        issued = it + 1;
+        item = item_end;
       }
-      if (*abort_flag) {
-        // drain: wait (bounded) for the copies still in flight before exiting
-        drain_wait(&ms.q_full, 0);
-        for (int it = max(0, issued - C::kStages); it < issued; ++it)
-          drain_wait(&ms.kv_full[it % C::kStages],
-                     static_cast<uint32_t>(it / C::kStages) & 1u);
+      if (abort_set(abort_flag)) {
+        // drain: wait (bounded) for the copies still in flight before exiting:
+        // the last Q load and the ring items issued last (items < g)
+        drain_wait(&ms.q_full, q_phase);
+        for (uint32_t it = g > C::kStages ? g - C::kStages : 0u; it < g; ++it)
+          drain_wait(&ms.kv_full[it % C::kStages], (it / C::kStages) & 1u);
       }
     }
   } else if (warp == kWarpMma) {
@@ -486,72 +521,89 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kTileDesc = C::kTileBytes >> 4;  // one tile in descriptor units
       // Descriptors are built once; every k-step only adds a constant to the
       // start-address field, so issuing an MMA costs a couple of instructions.
-      const uint64_t desc_q = sdesc_sw128(smem_u32(smem + C::kOffQ), 16, 1024);
-      const uint64_t desc_k = sdesc_sw128(smem_u32(smem + C::kOffKV), 16, 1024);
-      // V: bf16 MN-major (64-column chunks kBM * 128 bytes apart); e4m3 V^T K-major
-      const uint64_t desc_v =
-          sdesc_sw128(smem_u32(smem + C::kOffKV), kFp8 ? 16 : kBM * 128, 1024);
-      bool ok = mbar_wait(&ms.q_full, 0, abort_flag, p.err, kErrWaitMma, lim);
+      // Q and V differ from K by compile-time constants (start address; V:
+      // bf16 MN-major with 64-column chunks kBM * 128 bytes apart, e4m3 V^T
+      // K-major), so one descriptor stays live.
+      const uint32_t desc_k = sdesc_sw128_lo(smem_u32(smem + C::kOffKV), 16);
+      constexpr uint32_t kQFromK = static_cast<uint32_t>((C::kOffKV - C::kOffQ) >> 4);
+      constexpr uint32_t kVFromK = kFp8 ? 0u : static_cast<uint32_t>(((kBM * 128) >> 4) - 1) << 16;
+      constexpr uint32_t kS = C::kStages;  // power of two
+      static_assert((kS & (kS - 1)) == 0, "ring depth must be a power of two");
       // S_t = Q_t K^T from the K tile in ring slot `slot`
       auto issue_s = [&](int t, uint32_t slot) {
-        const uint64_t a0 = desc_q + static_cast<uint32_t>(t) * kTileDesc;
-        const uint64_t b0 = desc_k + slot * kTileDesc;
-        const uint32_t d = tmem + (t ? C::kColS1 : C::kColS0);
-        issue_s_steps<D, kFp8>(d, a0, b0, idesc_s);
+        const uint32_t a0 = desc_k - kQFromK + static_cast<uint32_t>(t) * kTileDesc;
+        if (t)
+          issue_s_steps<D, kFp8, C::kColS1>(tmem, a0, desc_k + slot * kTileDesc, idesc_s);
+        else
+          issue_s_steps<D, kFp8, C::kColS0>(tmem, a0, desc_k + slot * kTileDesc, idesc_s);
       };
       // O_t (+)= P_t V from the V tile in ring slot `slot`; P_t is in TMEM over S_t
       auto issue_pv = [&](int t, uint32_t slot, uint32_t acc) {
-        const uint64_t b0 = desc_v + slot * kTileDesc;
-        const uint32_t a = tmem + (t ? C::kColS1 : C::kColS0);
-        const uint32_t d = tmem + (t ? C::kColO1 : C::kColO0);
-        issue_pv_steps<kFp8>(d, a, b0, idesc_pv, acc);
+        const uint32_t b0 = desc_k + kVFromK + slot * kTileDesc;
+        if (t)
+          issue_pv_steps<kFp8, C::kColO1, C::kColS1>(tmem, b0, idesc_pv, acc);
+        else
+          issue_pv_steps<kFp8, C::kColO0, C::kColS0>(tmem, b0, idesc_pv, acc);
       };
-      // wait for P_t of KV tile jv (O_t is already rescaled when it arrives)
-      auto wait_p = [&](int t, int jv) -> bool {
-        if (!mbar_wait(&ms.p_full[t], jv & 1, abort_flag, p.err, kErrWaitMma, lim)) return false;
-        ATTN_TRACE_EV(5, t, jv);
+      int k = 0;  // units done
+      // wait for P_t of global step gs (O_t is already rescaled when it arrives)
+      auto wait_p = [&](int t, uint32_t gs, int jv) -> bool {
+        if (!mbar_wait(&ms.p_full[t], gs & 1u, abort_flag, p.err, kErrWaitMma, p.wait_limit_ns)) return false;
+        if (k == 0) ATTN_TRACE_EV(5, t, jv);
         tc_fence_after();
         return true;
       };
-      constexpr uint32_t kS = C::kStages;  // power of two
-      static_assert((kS & (kS - 1)) == 0, "ring depth must be a power of two");
-      for (int j = 0; j < n_kv && ok; ++j) {
-        const uint32_t itk = 2u * j, itv = 2u * j - 1u;
-        const uint32_t sk = itk % kS, sv = itv % kS;
-        ok = mbar_wait(&ms.kv_full[sk], (itk / kS) & 1u, abort_flag, p.err, kErrWaitMma, lim);
-        if (ok && j > 0)
-          ok = mbar_wait(&ms.kv_full[sv], (itv / kS) & 1u, abort_flag, p.err, kErrWaitMma, lim);
-        if (!ok) break;
-        tc_fence_after();
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (j > 0) {
-            ok = wait_p(t, j - 1);
-            if (!ok) break;
-            issue_pv(t, sv, j > 1 ? 1u : 0u);
-          }
-          issue_s(t, sk);
-          mma_commit(&ms.s_full[t]);
-          ATTN_TRACE_EV(6, t, j);
-        }
-        if (!ok) break;
-        mma_commit(&ms.kv_empty[sk]);
-        if (j > 0) mma_commit(&ms.kv_empty[sv]);
-      }
-      if (ok) {
-        const uint32_t itv = 2u * (n_kv - 1) + 1u;
-        const uint32_t sv = itv % kS;
-        ok = mbar_wait(&ms.kv_full[sv], (itv / kS) & 1u, abort_flag, p.err, kErrWaitMma, lim);
-        if (ok) {
+      uint32_t step = 0;  // key tiles of earlier units: ring items 2*step.., barrier phases
+      bool ok = true;
+      for (; ok; ++k) {
+        const int u = static_cast<int>(blockIdx.x + k * gridDim.x);
+        if (u >= ATTN_UNITS) break;
+        const uint32_t step_end = step + static_cast<uint32_t>(decode_unit(p, u, ATTN_NQB).n_kv);
+        ok = mbar_wait(&ms.q_full, k & 1, abort_flag, p.err, kErrWaitMma, p.wait_limit_ns);
+        // global step gs = step + j: K_j is ring item 2 gs, V_j item 2 gs + 1
+        for (uint32_t gs = step; gs < step_end && ok; ++gs) {
+          const uint32_t sk = (2u * gs) % kS, sv = (2u * gs - 1u) % kS;
+          ok = mbar_wait(&ms.kv_full[sk], ((2u * gs) / kS) & 1u, abort_flag, p.err, kErrWaitMma,
+                         p.wait_limit_ns);
+          if (ok && gs > step)
+            ok = mbar_wait(&ms.kv_full[sv], ((2u * gs - 1u) / kS) & 1u, abort_flag, p.err,
+                           kErrWaitMma, p.wait_limit_ns);
+          if (!ok) break;
           tc_fence_after();
           for (int t = 0; t < 2 && ok; ++t) {
-            ok = wait_p(t, n_kv - 1);
-            if (ok) {
-              issue_pv(t, sv, n_kv > 1 ? 1u : 0u);
-              mma_commit(&ms.o_done[t]);
+            if (gs > step) {
+              ok = wait_p(t, gs - 1, static_cast<int>(gs - step) - 1);
+              if (!ok) break;
+              issue_pv(t, sv, gs > step + 1 ? 1u : 0u);
             }
+            issue_s(t, sk);
+            mma_commit(&ms.s_full[t]);
+            if (k == 0) ATTN_TRACE_EV(6, t, gs - step);
           }
-          if (ok) mma_commit(&ms.kv_empty[sv]);
+          if (!ok) break;
+          mma_commit(&ms.kv_empty[sk]);
+          if (gs > step) mma_commit(&ms.kv_empty[sv]);
         }
+        // the unit's last Q K^T is issued: Q's buffers are free once it retires
+        if (ok) mma_commit(&ms.q_empty);
+        if (ok) {
+          const uint32_t gs = step_end - 1;
+          const uint32_t sv = (2u * gs + 1u) % kS;
+          ok = mbar_wait(&ms.kv_full[sv], ((2u * gs + 1u) / kS) & 1u, abort_flag, p.err,
+                         kErrWaitMma, p.wait_limit_ns);
+          if (ok) {
+            tc_fence_after();
+            for (int t = 0; t < 2 && ok; ++t) {
+              ok = wait_p(t, gs, static_cast<int>(gs - step));
+              if (ok) {
+                issue_pv(t, sv, gs > step ? 1u : 0u);
+                mma_commit(&ms.o_done[t]);
+              }
+            }
+            if (ok) mma_commit(&ms.kv_empty[sv]);
+          }
+        }
+        step = step_end;
       }
       // all issued MMAs retire before the CTA releases TMEM
       mma_commit(&ms.mma_done);
@@ -585,20 +637,29 @@ cudaError_t launch_d(const FwdParams& p_in, cudaStream_t stream) {
   FwdParams p = p_in;
   p.group_heads = causal_group_heads(p);
   using C = Cfg<D, kFp8>;
-  // the shared-memory opt-in is a per-device property of the function
-  static std::atomic<bool> attr_done[64];  // zero-initialised: false
+  // per device, once: the shared-memory opt-in (a property of the function
+  // on that device) and the SM count
+  static std::atomic<int> sm_count[64];  // zero-initialised: not yet set up
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_done[dev].load(std::memory_order_acquire)) {
+  int sms = sm_count[dev].load(std::memory_order_acquire);
+  if (sms == 0) {
     e = cudaFuncSetAttribute(attn_fwd_kernel<D, kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_done[dev].store(true, std::memory_order_release);
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    sm_count[dev].store(sms, std::memory_order_release);
   }
+  // Non-causal: one CTA per SM (1 CTA fits an SM), each working through
+  // units of equal length.  Causal: one CTA per unit, so that the block
+  // scheduler, which hands the next unit to whichever SM frees first,
+  // balances the units' different lengths.
   const long long nqb = (p.Nq + 2 * kBM - 1) / (2 * kBM);
-  const long long grid = nqb * p.B * p.Hq;
+  const long long units = nqb * p.B * p.Hq;
+  const long long grid = (p.causal || units < sms) ? units : sms;
   attn_fwd_kernel<D, kFp8><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }

@@ -20,9 +20,10 @@ enum : unsigned int {
 // Forward (prefill) launch parameters.  Tensor maps are 3-D views with a
 // 128-byte swizzle: bf16 [B*H, N, D] with box {64, 128, 1}; for FP8, e4m3
 // Q and K [B*H, N, D] with box {128, 128, 1} and V^T [B*Hkv, D, Nk] with box
-// {128 keys, 128 rows, 1}; O is always bf16.
+// {128 keys, 128 rows, 1}.
 struct FwdParams {
-  CUtensorMap tmap_q, tmap_k, tmap_v, tmap_o;
+  CUtensorMap tmap_q, tmap_k, tmap_v;
+  void* o;             // [B, Hq, Nq, D] bf16
   float* lse;          // [B, Hq, Nq] fp32
   int B, Hq, Hkv, Nq, Nk, D;
   int causal;

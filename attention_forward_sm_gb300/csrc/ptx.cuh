@@ -1,4 +1,4 @@
-// Inline-PTX building blocks for sm_103a: mbarrier pipes, TMA tile copies,
+// Inline-PTX building blocks for sm_103a: mbarrier pipes, TMA tile loads,
 // tcgen05 (tensor-core MMA with TMEM accumulators) and TMEM load/store.
 //
 // Everything here is a thin wrapper over one PTX instruction (or a fixed
@@ -51,21 +51,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase with the given parity.  Returns true when the
-// phase completed.  Gives up (returns false) when `abort` is already set by
-// another role, or after `limit_ns` of wall time, in which case it sets
-// `abort`, ORs `site` into the device error word `err` and returns false.
+// phase completed.  Gives up (returns false) when the abort flag (an int in
+// shared memory at shared-window address `abort_sa`) is already set by
+// another role, or after `limit_ns` of wall time, in which case it sets the
+// flag, ORs `site` into the device error word `err` and returns false.
 // Every role that sees false leaves its loop, so the CTA drains and exits
 // instead of hanging.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+__device__ __forceinline__ bool abort_set(uint32_t abort_sa) {
+  int v;
+  asm volatile("ld.volatile.shared.b32 %0, [%1];" : "=r"(v) : "r"(abort_sa) : "memory");
+  return v != 0;
+}
+__device__ __forceinline__ void abort_raise(uint32_t abort_sa) {
+  asm volatile("st.volatile.shared.b32 [%0], %1;" ::"r"(abort_sa), "r"(1) : "memory");
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t abort_sa,
                                           unsigned int* err, uint32_t site, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0u) {
-      if (*abort) return false;
+      if (abort_set(abort_sa)) return false;
       if (globaltimer_ns() - t0 > limit_ns) {
-        *abort = 1;
+        abort_raise(abort_sa);
         atomicOr(err, site);
         return false;
       }
@@ -88,26 +97,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
-// 3-D tiled store shared -> global (rows outside the tensor are clipped).
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0,
-                                             int c1, int c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
-          map),
-      "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(src))
-      : "memory");
-}
-__device__ __forceinline__ void tma_store_commit() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void tma_store_wait_all0() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-// Generic-proxy shared-memory writes made visible to the async (TMA) proxy.
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
@@ -117,11 +106,6 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
-}
-
-// ---------------------------------------------------------------- named barriers
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // ---------------------------------------------------------------- register reallocation
@@ -179,68 +163,72 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t M, uint32_t N) {
 //   aligned), [61,64) swizzle mode (2 = 128B).
 // K-major: rows of 128 B, 8-row groups `sbo` apart (lbo unused).
 // MN-major: 64-element MN chunks `lbo` apart, 8-row K groups `sbo` apart.
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
-  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
-  d |= static_cast<uint64_t>(1) << 46;
-  d |= static_cast<uint64_t>(2) << 61;
-  return d;
+// Every descriptor of these kernels has sbo = 1024, so the upper word
+// (kSdescHi) is the same for all; only the lower word (start address,
+// leading byte offset) varies, and the MMA wrappers take that 32-bit word and
+// rebuild the descriptor inside the instruction group.
+constexpr uint64_t kSdescHi = (static_cast<uint64_t>(1024 >> 4) << 32) |
+                              (static_cast<uint64_t>(1) << 46) | (static_cast<uint64_t>(2) << 61);
+__device__ __forceinline__ uint32_t sdesc_sw128_lo(uint32_t saddr, uint32_t lbo) {
+  return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
 }
 
-// D[tmem] (+)= A[smem desc] * B[smem desc] (mma_ss_off) or A[tmem] * B[smem
-// desc] (mma_ts_off), kind::f16.  A compile-time offset (in 16-byte
-// descriptor units) is added to the start address of the shared-memory
-// descriptors inside the instruction group, so the compiler keeps one base
-// descriptor live instead of one per k-step.
-template <uint32_t kOffA, uint32_t kOffB>
-__device__ __forceinline__ void mma_ss_off(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                           uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
-      "add.s64 da, %1, %5;\n\t"
-      "add.s64 db, %2, %6;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "n"(kOffA), "n"(kOffB)
-      : "memory");
+// D[tmem] (+)= A[smem desc] * B[smem desc] (mma_ss) or A[tmem] * B[smem
+// desc] (mma_ts), kind::f16 (bf16 operands) or kind::f8f6f4 (e4m3).  Every
+// per-instruction offset is a compile-time constant added inside the
+// instruction group -- TMEM columns of D (and of A for mma_ts) to the TMEM
+// base, 16-byte descriptor units to the descriptors' start addresses -- so
+// an unrolled sequence of MMAs keeps only the TMEM base and one descriptor
+// word live.
+#define ATTN_MMA_SS(KIND)                                                                    \
+  asm volatile(                                                                             \
+      "{\n\t.reg .pred p;\n\t.reg .b32 dt, al, bl;\n\t.reg .b64 da, db;\n\t"           \
+      "add.u32 dt, %0, %5;\n\t"                                                           \
+      "add.u32 al, %1, %6;\n\t"                                                           \
+      "add.u32 bl, %2, %7;\n\t"                                                           \
+      "cvt.u64.u32 da, al;\n\t"                                                           \
+      "cvt.u64.u32 db, bl;\n\t"                                                           \
+      "or.b64 da, da, %8;\n\t"                                                            \
+      "or.b64 db, db, %8;\n\t"                                                            \
+      "setp.ne.b32 p, %4, 0;\n\t"                                                         \
+      "tcgen05.mma.cta_group::1." KIND " [dt], da, db, %3, p;\n\t}" ::"r"(tmem),            \
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(kColD), "n"(kOffA), "n"(kOffB), \
+      "n"(kSdescHi)                                                                         \
+      : "memory")
+#define ATTN_MMA_TS(KIND)                                                                    \
+  asm volatile(                                                                             \
+      "{\n\t.reg .pred p;\n\t.reg .b32 dt, at, bl;\n\t.reg .b64 db;\n\t"               \
+      "add.u32 dt, %0, %4;\n\t"                                                           \
+      "add.u32 at, %0, %5;\n\t"                                                           \
+      "add.u32 bl, %1, %6;\n\t"                                                           \
+      "cvt.u64.u32 db, bl;\n\t"                                                           \
+      "or.b64 db, db, %7;\n\t"                                                            \
+      "setp.ne.b32 p, %3, 0;\n\t"                                                         \
+      "tcgen05.mma.cta_group::1." KIND " [dt], [at], db, %2, p;\n\t}" ::"r"(tmem),          \
+      "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(kColD), "n"(kColA), "n"(kOffB),           \
+      "n"(kSdescHi)                                                                         \
+      : "memory")
+// D at TMEM column kColD, A and B descriptors (lower words) + kOffA, kOffB
+template <bool kF8, uint32_t kColD, uint32_t kOffA, uint32_t kOffB>
+__device__ __forceinline__ void mma_ss(uint32_t tmem, uint32_t a_lo, uint32_t b_lo,
+                                       uint32_t idesc, uint32_t accumulate) {
+  if constexpr (kF8)
+    ATTN_MMA_SS("kind::f8f6f4");
+  else
+    ATTN_MMA_SS("kind::f16");
 }
-template <uint32_t kOffB>
-__device__ __forceinline__ void mma_ts_off(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                           uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
-      "add.s64 db, %2, %5;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "n"(kOffB)
-      : "memory");
+// D at TMEM column kColD, A at TMEM column kColA, B descriptor (lower word) + kOffB
+template <bool kF8, uint32_t kColD, uint32_t kColA, uint32_t kOffB>
+__device__ __forceinline__ void mma_ts(uint32_t tmem, uint32_t b_lo, uint32_t idesc,
+                                       uint32_t accumulate) {
+  if constexpr (kF8)
+    ATTN_MMA_TS("kind::f8f6f4");
+  else
+    ATTN_MMA_TS("kind::f16");
 }
-// kind::f8f6f4 (e4m3 operands, K = 32 per instruction) versions of the two above.
-template <uint32_t kOffA, uint32_t kOffB>
-__device__ __forceinline__ void mma_ss_off_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                              uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
-      "add.s64 da, %1, %5;\n\t"
-      "add.s64 db, %2, %6;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "n"(kOffA), "n"(kOffB)
-      : "memory");
-}
-template <uint32_t kOffB>
-__device__ __forceinline__ void mma_ts_off_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                              uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
-      "add.s64 db, %2, %5;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], db, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "n"(kOffB)
-      : "memory");
-}
+#undef ATTN_MMA_SS
+#undef ATTN_MMA_TS
+
 // Arrive on `bar` once every tcgen05 op issued so far by this thread completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
@@ -277,6 +265,16 @@ __device__ __forceinline__ void tmem_ld_pair32(uint32_t taddr, uint32_t (&r)[32]
       "%28, %29, %30, %31}, [%32], %33;\n\t"
       "tcgen05.wait::ld.sync.aligned;"
       : ATTN_R8(0), ATTN_R8(8), ATTN_R8(16), ATTN_R8(24)
+      : "r"(taddr), "n"(kHalf)
+      : "memory");
+}
+template <uint32_t kHalf>
+__device__ __forceinline__ void tmem_ld_pair16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16], %17;\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : ATTN_R8(0), ATTN_R8(8)
       : "r"(taddr), "n"(kHalf)
       : "memory");
 }
