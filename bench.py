@@ -363,6 +363,12 @@ def run_gpu(args):
         "gpu_launches": 3 * K,
         "clocks": clocks,
         "prefill_ms_per_call": 1e3 * pf_avg_s,
+        # spread of the per-call prefill times over the timed steps (clock and
+        # power behaviour under sustained load shows here)
+        "prefill_ms_per_call_stats": {"min": min(pf_ms), "median": statistics.median(pf_ms),
+                                      "max": max(pf_ms),
+                                      "first_quarter_mean": statistics.mean(pf_ms[:max(1, K // 4)]),
+                                      "last_quarter_mean": statistics.mean(pf_ms[-max(1, K // 4):])},
         "other_prefill_workloads": other,
         "decode_graph": dec_graph,
     }
