@@ -53,6 +53,7 @@ constexpr int kBN = 128;          // keys per K/V tile
 constexpr int kThreads = 640;     // 20 warps: 16 softmax/epilogue + load, MMA, 2 idle
 constexpr int kWarpLoad = 16;
 constexpr int kWarpMma = 17;
+constexpr int kClcReaders = 18;   // loader, MMA issuer, 16 softmax warps
 // setmaxnreg split of the 61440 registers the launch gets (640 threads x 96):
 // 4 softmax warpgroups + 1 warpgroup for load / MMA / idle warps.
 constexpr uint32_t kRegSoftmax = 112, kRegOther = 32;
@@ -91,6 +92,9 @@ struct Misc {
   uint64_t o_done[2];     // every MMA of the unit's O_t retired (one phase per unit)
   uint64_t mma_done;
   uint64_t kv_full[8], kv_empty[8];
+  uint64_t clc_full[2];   // next-unit response k in slot k % 2 arrived
+  uint64_t clc_empty[2];  // every role has read response k (kClcReaders arrivals)
+  uint4 clc_resp[2];      // cluster-launch-control responses
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -192,9 +196,12 @@ __device__ __forceinline__ int kv_head(const FwdParams& p, int bh) {
   return (bh / p.Hq) * p.Hkv + (bh % p.Hq) / (p.Hq / p.Hkv);
 }
 
-// Each CTA works through units blockIdx.x, blockIdx.x + gridDim.x, ... (one
-// unit when the grid covers them all; a persistent grid of one CTA per SM
-// otherwise).  TMEM, barriers and the K/V ring live across units: every
+// The grid has one CTA per unit, in unit order, but a running CTA takes over
+// CTAs that have not started yet (cluster launch control) and does their
+// units itself, in the order the hardware would have started them: the
+// loader asks for the next unit once it has issued the current unit's
+// loads, and every role reads the answer (response k in slot k % 2) when it
+// finishes unit k.  TMEM, barriers and the K/V ring live across units: every
 // barrier phase and the ring position run on, so the next unit's K/V and Q
 // loads and its first Q K^T overlap the current unit's last steps and
 // epilogue.
@@ -225,6 +232,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ms.o_done[t], 1);
     }
     mbar_init(&ms.mma_done, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ms.clc_full[i], 1);
+      mbar_init(&ms.clc_empty[i], kClcReaders);
+    }
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&ms.kv_full[s], 1);
       mbar_init(&ms.kv_empty[s], 1);
@@ -275,8 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool tracer = (warp & 7) == 0 && lane == 0;
     uint32_t step = 0;  // key tiles of this CTA's earlier units: barrier phases run on
     bool ok = true;
-    for (int u = static_cast<int>(blockIdx.x), k = 0; u < ATTN_UNITS && ok;
-         u += static_cast<int>(gridDim.x), ++k) {
+    for (int u = static_cast<int>(blockIdx.x), k = 0; u >= 0 && ok; ++k) {
       const Unit w = decode_unit(p, u, ATTN_NQB);
       const int tile_row0 = w.q_base + t * kBM;
       const int row = tile_row0 + r;
@@ -439,6 +449,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (c == 0 && row < p.Nq)
         p.lse[static_cast<size_t>(w.bh) * p.Nq + row] =
             (m - C::kPBias + __log2f(l_row)) * 0.69314718055994530942f;
+      // the next unit: response k
+      if (!warp_all(mbar_wait(&ms.clc_full[k & 1], (k >> 1) & 1, abort_flag, p.err,
+                              kErrWaitCorr, p.wait_limit_ns))) {
+        ok = false;
+        break;
+      }
+      const int nu = clc_response_ctaid_x(smem_u32(&ms.clc_resp[k & 1]));
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ms.clc_empty[k & 1]);
+      u = nu < ATTN_UNITS ? nu : -1;
     }
   } else if (warp == kWarpLoad) {
     // =====================================================================
@@ -452,9 +473,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t g = 1;       // next ring item (the first unit's K_0 was issued during setup)
       uint32_t q_phase = 0;  // q_full phase of the last Q load issued
       bool ok = true;
+      int clc_k = -1;        // last next-unit request issued
+      int u = static_cast<int>(blockIdx.x);
       for (int k = 0; ok; ++k) {
-        const int u = static_cast<int>(blockIdx.x + k * gridDim.x);
-        if (u >= ATTN_UNITS) break;
         const Unit w = decode_unit(p, u, ATTN_NQB);
         const int bhkv = kv_head(p, w.bh);
         const uint32_t item_end = item + 2u * static_cast<uint32_t>(w.n_kv);
@@ -500,11 +521,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         item = item_end;
+        if (!ok) break;
+        // every load of unit k is issued: ask for the next unit (slot k % 2,
+        // free once every role has read response k - 2)
+        if (k >= 2 && !mbar_wait(&ms.clc_empty[k & 1], ((k >> 1) + 1) & 1, abort_flag, p.err,
+                                 kErrWaitLoad, p.wait_limit_ns)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&ms.clc_full[k & 1], 16);
+        clc_try_cancel(smem_u32(&ms.clc_resp[k & 1]), &ms.clc_full[k & 1]);
+        clc_k = k;
+        if (!mbar_wait(&ms.clc_full[k & 1], (k >> 1) & 1, abort_flag, p.err, kErrWaitLoad,
+                       p.wait_limit_ns)) {
+          ok = false;
+          break;
+        }
+        const int nu = clc_response_ctaid_x(smem_u32(&ms.clc_resp[k & 1]));
+        fence_proxy_async_smem();
+        mbar_arrive(&ms.clc_empty[k & 1]);
+        if (nu < 0 || nu >= ATTN_UNITS) break;
+        u = nu;
       }
       if (abort_set(abort_flag)) {
         // drain: wait (bounded) for the copies still in flight before exiting:
         // the last Q load and the ring items issued last (items < g)
         drain_wait(&ms.q_full, q_phase);
+        if (clc_k >= 0) drain_wait(&ms.clc_full[clc_k & 1], (clc_k >> 1) & 1);
         for (uint32_t it = g > C::kStages ? g - C::kStages : 0u; it < g; ++it)
           drain_wait(&ms.kv_full[it % C::kStages], (it / C::kStages) & 1u);
       }
@@ -555,9 +598,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       uint32_t step = 0;  // key tiles of earlier units: ring items 2*step.., barrier phases
       bool ok = true;
+      int u = static_cast<int>(blockIdx.x);
       for (; ok; ++k) {
-        const int u = static_cast<int>(blockIdx.x + k * gridDim.x);
-        if (u >= ATTN_UNITS) break;
         const uint32_t step_end = step + static_cast<uint32_t>(decode_unit(p, u, ATTN_NQB).n_kv);
         ok = mbar_wait(&ms.q_full, k & 1, abort_flag, p.err, kErrWaitMma, p.wait_limit_ns);
         // global step gs = step + j: K_j is ring item 2 gs, V_j item 2 gs + 1
@@ -604,6 +646,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         step = step_end;
+        if (!ok) break;
+        // the next unit: response k
+        ok = mbar_wait(&ms.clc_full[k & 1], (k >> 1) & 1, abort_flag, p.err, kErrWaitMma,
+                       p.wait_limit_ns);
+        if (!ok) break;
+        const int nu = clc_response_ctaid_x(smem_u32(&ms.clc_resp[k & 1]));
+        fence_proxy_async_smem();
+        mbar_arrive(&ms.clc_empty[k & 1]);
+        if (nu < 0 || nu >= ATTN_UNITS) break;
+        u = nu;
       }
       // all issued MMAs retire before the CTA releases TMEM
       mma_commit(&ms.mma_done);
@@ -619,6 +671,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
+#undef ATTN_NQB
+#undef ATTN_UNITS
 }
 
 // Causal unit order: query heads per group, whole KV-head groups, so that
@@ -637,29 +691,21 @@ cudaError_t launch_d(const FwdParams& p_in, cudaStream_t stream) {
   FwdParams p = p_in;
   p.group_heads = causal_group_heads(p);
   using C = Cfg<D, kFp8>;
-  // per device, once: the shared-memory opt-in (a property of the function
-  // on that device) and the SM count
-  static std::atomic<int> sm_count[64];  // zero-initialised: not yet set up
+  // the shared-memory opt-in is a per-device property of the function
+  static std::atomic<bool> attr_done[64];  // zero-initialised: false
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  int sms = sm_count[dev].load(std::memory_order_acquire);
-  if (sms == 0) {
+  if (!attr_done[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(attn_fwd_kernel<D, kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    sm_count[dev].store(sms, std::memory_order_release);
+    attr_done[dev].store(true, std::memory_order_release);
   }
-  // Non-causal: one CTA per SM (1 CTA fits an SM), each working through
-  // units of equal length.  Causal: one CTA per unit, so that the block
-  // scheduler, which hands the next unit to whichever SM frees first,
-  // balances the units' different lengths.
+  // one CTA per unit; running CTAs take over the ones not started yet
   const long long nqb = (p.Nq + 2 * kBM - 1) / (2 * kBM);
-  const long long units = nqb * p.B * p.Hq;
-  const long long grid = (p.causal || units < sms) ? units : sms;
+  const long long grid = nqb * p.B * p.Hq;
   attn_fwd_kernel<D, kFp8><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }

@@ -97,6 +97,38 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// Generic-proxy shared-memory accesses ordered before later async-proxy ones.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- cluster launch control
+// Asks the hardware to cancel a CTA of this grid that has not started yet
+// and to hand its work to the calling CTA: the 16-byte response lands at
+// shared address `resp` and completes 16 transaction bytes on `bar`.
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint64_t* bar) {
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 "
+      "[%0], [%1];" ::"r"(resp),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+// Reads a response: the x block index of the CTA taken over, or -1 when the
+// request found no CTA left to take.
+__device__ __forceinline__ int clc_response_ctaid_x(uint32_t resp) {
+  uint32_t ok, x = 0;
+  asm volatile(
+      "{\n\t.reg .b128 r;\n\t.reg .pred p;\n\t"
+      "ld.shared.b128 r, [%2];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t"
+      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t}"
+      : "=r"(ok), "+r"(x)
+      : "r"(resp)
+      : "memory");
+  return ok ? static_cast<int>(x) : -1;
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
