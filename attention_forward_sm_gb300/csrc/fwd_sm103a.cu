@@ -419,7 +419,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       step += w.n_kv;
       // ---- epilogue of tile t: O / l -> bf16 -> global (a thread writes the
-      // D/2 columns it owns of its row), and LSE.  The TMEM reads of O_t
+      // D/2 columns it owns of its row; evict-first in L2, since nothing here
+      // reads O again and the K/V tiles being reused should keep the space),
+      // and LSE.  The TMEM reads of O_t
       // complete here, before these warps publish the next unit's first P of
       // this tile, which the MMA that overwrites O_t waits for.
       ok = ok && warp_all(mbar_wait(&ms.o_done[t], k & 1, abort_flag, p.err, kErrWaitCorr, p.wait_limit_ns));
@@ -443,7 +445,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (row < p.Nq) {
 #pragma unroll
           for (int g = 0; g < 4; ++g)
-            orow[kk * 4 + g] = make_uint4(wv[4 * g], wv[4 * g + 1], wv[4 * g + 2], wv[4 * g + 3]);
+            st_global_v4_evict_first(orow + kk * 4 + g, wv[4 * g], wv[4 * g + 1], wv[4 * g + 2],
+                                     wv[4 * g + 3]);
         }
       }
       if (c == 0 && row < p.Nq)

@@ -139,6 +139,16 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
+// 16-byte global store marked evict-first in L2.
+__device__ __forceinline__ void st_global_v4_evict_first(void* addr, uint32_t a, uint32_t b,
+                                                         uint32_t c, uint32_t d) {
+  asm volatile(
+      "{\n\t.reg .b64 pol;\n\t"
+      "createpolicy.fractional.L2::evict_first.b64 pol, 1.0;\n\t"
+      "st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, pol;\n\t}" ::"l"(addr),
+      "r"(a), "r"(b), "r"(c), "r"(d)
+      : "memory");
+}
 
 // ---------------------------------------------------------------- register reallocation
 template <uint32_t N>

@@ -374,3 +374,50 @@ def test_correction_path(shape, construction):
         bound = 2.0 ** -8 * np.abs(ref) + 1e-4 * v.float().abs().max().item()
         bad = np.abs(og - ref) > bound
         assert not bad.any(), f"{label}: {int(bad.sum())} elements over the tight bound"
+
+
+# ----------------------------------------------------------------------------- unit scheduling
+#
+# The prefill grid has one CTA per (batch*head, query-tile pair) unit, and
+# running CTAs take over the ones not started yet (cluster launch control),
+# so a CTA works through several units with its barriers and K/V ring
+# carried over.  These check every output row when there are several times
+# more units than SMs, and two launches running at once on two streams.
+
+
+@pytest.mark.parametrize("shape", [(2, 16, 4, 1536, 1536, 128, True), (1, 64, 64, 2048, 2048, 64, False),
+                                   (3, 32, 8, 640, 2000, 128, False)],
+                         ids=lambda s: "B{}Hq{}Hkv{}Nq{}Nk{}D{}{}".format(*s[:6], "c" if s[6] else ""))
+def test_many_units_every_row(shape):
+    B, Hq, Hkv, Nq, Nk, D, causal = shape
+    w = W.custom(B, Hq, Hkv, Nq, Nk, D, causal, seed_index=1400 + Nq % 97)
+    units = B * Hq * ((Nq + 255) // 256)
+    assert units > 152
+    q, k, v = (t.cuda() for t in W.make_inputs(w, "cpu"))
+    o, lse = run_prefill(w, q, k, v)
+    assert attn.attn_get_device_error() == 0
+    o_ref, lse_ref = oracle_prefill(w, q, k, v)
+    check(o, lse, o_ref.reshape(o.shape), lse_ref.reshape(lse.shape), f"{units} units")
+
+
+def test_two_streams_at_once():
+    """Two different problems launched back to back on two streams, with no
+    ordering between them, run concurrently; each grid's CTAs take over only
+    its own units, so both results match the oracle."""
+    w1 = W.custom(2, 16, 16, 2048, 2048, 128, False, seed_index=1500)
+    w2 = W.custom(1, 16, 4, 3000, 3000, 64, True, seed_index=1501)
+    data = []
+    for w in (w1, w2):
+        q, k, v = (t.cuda() for t in W.make_inputs(w, "cpu"))
+        data.append((w, q, k, v, torch.empty_like(q),
+                     torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device="cuda")))
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for _ in range(3):
+        for s, (w, q, k, v, o, lse) in zip(streams, data):
+            attn.attn_fwd(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.D, w.causal, w.scale, s)
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_error() == 0
+    for (w, q, k, v, o, lse) in data:
+        o_ref, lse_ref = oracle_prefill(w, q, k, v)
+        check(o, lse, o_ref.reshape(o.shape), lse_ref.reshape(lse.shape), w.label())
