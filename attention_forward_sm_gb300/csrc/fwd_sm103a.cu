@@ -9,11 +9,12 @@
 // Kernels", introduction).  Each query row keeps a running max m and running
 // sum l; when m grows the accumulated output is rescaled ("correction"
 // partition in "Warp Specialization in Triton: Design and Roadmap", "How the
-// compiler does it").  The kernel is warp-specialised: load, MMA, softmax,
-// correction and epilogue run in different warps and talk through mbarrier
-// producer/consumer pipes, so loads, tensor-core work and exponentials
-// overlap (same note, and the pipeline diagram and "Hardware Mechanics" of the
-// FlashAttention-3 page, which describe the Hopper version of the idea).
+// compiler does it").  The kernel is warp-specialised: loads, MMAs and the
+// softmax (with the correction and the epilogue) run in different warps and
+// talk through mbarrier producer/consumer pipes, so loads, tensor-core work
+// and exponentials overlap (same note, and the pipeline diagram and
+// "Hardware Mechanics" of the FlashAttention-3 page, which describe the
+// Hopper version of the idea).
 //
 // GB300 design (not the Hopper layout of the pages):
 //   * one CTA = 2 query tiles of 128 rows of one (batch, head); the two tiles
@@ -34,9 +35,10 @@
 //     (otherwise the stale max stays: exact, because the final division uses
 //     the same max), and run the epilogue (O / l -> bf16 -> global, and LSE);
 //   * setmaxnreg moves registers from the load/MMA warps to the softmax warps;
-//   * a CTA may work through several units in turn (non-causal: one CTA per
-//     SM), its TMEM, barriers and K/V ring carrying over, so the next unit's
-//     loads and first Q K^T overlap the current unit's tail.
+//   * a running CTA takes over CTAs that have not started yet (cluster
+//     launch control) and works through their units in turn, its TMEM,
+//     barriers and K/V ring carrying over, so the next unit's loads and first
+//     Q K^T overlap the current unit's tail.
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
