@@ -559,10 +559,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kWarpMma) {
     // =====================================================================
-    // MMA issuer (one thread): S_t = Q_t K_j^T, O_t += P_t V_j
+    // MMA issuer: S_t = Q_t K_j^T, O_t += P_t V_j.  The whole warp runs this
+    // loop (waits are warp-wide votes, so control flow stays uniform); one
+    // elected thread issues each MMA and commit.
     // =====================================================================
     reg_dealloc<kRegOther>();
-    if (lane == 0) {
+    {
       constexpr uint32_t idesc_s =
           kFp8 ? idesc_e4m3_f32(128, kBN) : idesc_bf16_f32(128, kBN, false);
       constexpr uint32_t idesc_pv = kFp8 ? idesc_e4m3_f32(128, D) : idesc_bf16_f32(128, D, true);
@@ -596,8 +598,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       int k = 0;  // units done
       // wait for P_t of global step gs (O_t is already rescaled when it arrives)
       auto wait_p = [&](int t, uint32_t gs, int jv) -> bool {
-        if (!mbar_wait(&ms.p_full[t], gs & 1u, abort_flag, p.err, kErrWaitMma, p.wait_limit_ns)) return false;
-        if (k == 0) ATTN_TRACE_EV(5, t, jv);
+        if (!warp_all(mbar_wait(&ms.p_full[t], gs & 1u, abort_flag, p.err, kErrWaitMma,
+                                p.wait_limit_ns)))
+          return false;
+        if (lane == 0 && k == 0) ATTN_TRACE_EV(5, t, jv);
         tc_fence_after();
         return true;
       };
@@ -606,15 +610,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       int u = static_cast<int>(blockIdx.x);
       for (; ok; ++k) {
         const uint32_t step_end = step + static_cast<uint32_t>(decode_unit(p, u, ATTN_NQB).n_kv);
-        ok = mbar_wait(&ms.q_full, k & 1, abort_flag, p.err, kErrWaitMma, p.wait_limit_ns);
+        ok = warp_all(mbar_wait(&ms.q_full, k & 1, abort_flag, p.err, kErrWaitMma, p.wait_limit_ns));
         // global step gs = step + j: K_j is ring item 2 gs, V_j item 2 gs + 1
         for (uint32_t gs = step; gs < step_end && ok; ++gs) {
           const uint32_t sk = (2u * gs) % kS, sv = (2u * gs - 1u) % kS;
-          ok = mbar_wait(&ms.kv_full[sk], ((2u * gs) / kS) & 1u, abort_flag, p.err, kErrWaitMma,
-                         p.wait_limit_ns);
+          ok = warp_all(mbar_wait(&ms.kv_full[sk], ((2u * gs) / kS) & 1u, abort_flag, p.err,
+                                  kErrWaitMma, p.wait_limit_ns));
           if (ok && gs > step)
-            ok = mbar_wait(&ms.kv_full[sv], ((2u * gs - 1u) / kS) & 1u, abort_flag, p.err,
-                           kErrWaitMma, p.wait_limit_ns);
+            ok = warp_all(mbar_wait(&ms.kv_full[sv], ((2u * gs - 1u) / kS) & 1u, abort_flag, p.err,
+                                    kErrWaitMma, p.wait_limit_ns));
           if (!ok) break;
           tc_fence_after();
           for (int t = 0; t < 2 && ok; ++t) {
@@ -625,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             issue_s(t, sk);
             mma_commit(&ms.s_full[t]);
-            if (k == 0) ATTN_TRACE_EV(6, t, gs - step);
+            if (lane == 0 && k == 0) ATTN_TRACE_EV(6, t, gs - step);
           }
           if (!ok) break;
           mma_commit(&ms.kv_empty[sk]);
@@ -636,8 +640,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) {
           const uint32_t gs = step_end - 1;
           const uint32_t sv = (2u * gs + 1u) % kS;
-          ok = mbar_wait(&ms.kv_full[sv], ((2u * gs + 1u) / kS) & 1u, abort_flag, p.err,
-                         kErrWaitMma, p.wait_limit_ns);
+          ok = warp_all(mbar_wait(&ms.kv_full[sv], ((2u * gs + 1u) / kS) & 1u, abort_flag, p.err,
+                                  kErrWaitMma, p.wait_limit_ns));
           if (ok) {
             tc_fence_after();
             for (int t = 0; t < 2 && ok; ++t) {
@@ -653,12 +657,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         step = step_end;
         if (!ok) break;
         // the next unit: response k
-        ok = mbar_wait(&ms.clc_full[k & 1], (k >> 1) & 1, abort_flag, p.err, kErrWaitMma,
-                       p.wait_limit_ns);
+        ok = warp_all(mbar_wait(&ms.clc_full[k & 1], (k >> 1) & 1, abort_flag, p.err, kErrWaitMma,
+                                p.wait_limit_ns));
         if (!ok) break;
         const int nu = clc_response_ctaid_x(smem_u32(&ms.clc_resp[k & 1]));
         fence_proxy_async_smem();
-        mbar_arrive(&ms.clc_empty[k & 1]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ms.clc_empty[k & 1]);
         if (nu < 0 || nu >= ATTN_UNITS) break;
         u = nu;
       }

@@ -221,10 +221,18 @@ __device__ __forceinline__ uint32_t sdesc_sw128_lo(uint32_t saddr, uint32_t lbo)
 // instruction group -- TMEM columns of D (and of A for mma_ts) to the TMEM
 // base, 16-byte descriptor units to the descriptors' start addresses -- so
 // an unrolled sequence of MMAs keeps only the TMEM base and one descriptor
-// word live.
+// word live.  The whole (converged) warp executes these wrappers with
+// warp-uniform operands, and elect.sync picks the one thread that issues:
+// issued that way an MMA costs the warp far fewer cycles than from a
+// single-thread branch (one thread's issue of an N = 64 MMA took about as
+// long as an N = 128 one), and the issue rate holds up next to busy warps
+// on the same SMSP.  elect.sync elects the same thread every time for the
+// same member mask (the full warp here), so mma_commit, elected the same
+// way, is issued by the thread that issued the MMAs it tracks.
 #define ATTN_MMA_SS(KIND)                                                                    \
   asm volatile(                                                                             \
-      "{\n\t.reg .pred p;\n\t.reg .b32 dt, al, bl;\n\t.reg .b64 da, db;\n\t"           \
+      "{\n\t.reg .pred p, e;\n\t.reg .b32 dt, al, bl;\n\t.reg .b64 da, db;\n\t"        \
+      "elect.sync _|e, 0xffffffff;\n\t"                                                   \
       "add.u32 dt, %0, %5;\n\t"                                                           \
       "add.u32 al, %1, %6;\n\t"                                                           \
       "add.u32 bl, %2, %7;\n\t"                                                           \
@@ -233,20 +241,21 @@ __device__ __forceinline__ uint32_t sdesc_sw128_lo(uint32_t saddr, uint32_t lbo)
       "or.b64 da, da, %8;\n\t"                                                            \
       "or.b64 db, db, %8;\n\t"                                                            \
       "setp.ne.b32 p, %4, 0;\n\t"                                                         \
-      "tcgen05.mma.cta_group::1." KIND " [dt], da, db, %3, p;\n\t}" ::"r"(tmem),            \
+      "@e tcgen05.mma.cta_group::1." KIND " [dt], da, db, %3, p;\n\t}" ::"r"(tmem),         \
       "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(kColD), "n"(kOffA), "n"(kOffB), \
       "n"(kSdescHi)                                                                         \
       : "memory")
 #define ATTN_MMA_TS(KIND)                                                                    \
   asm volatile(                                                                             \
-      "{\n\t.reg .pred p;\n\t.reg .b32 dt, at, bl;\n\t.reg .b64 db;\n\t"               \
+      "{\n\t.reg .pred p, e;\n\t.reg .b32 dt, at, bl;\n\t.reg .b64 db;\n\t"            \
+      "elect.sync _|e, 0xffffffff;\n\t"                                                   \
       "add.u32 dt, %0, %4;\n\t"                                                           \
       "add.u32 at, %0, %5;\n\t"                                                           \
       "add.u32 bl, %1, %6;\n\t"                                                           \
       "cvt.u64.u32 db, bl;\n\t"                                                           \
       "or.b64 db, db, %7;\n\t"                                                            \
       "setp.ne.b32 p, %3, 0;\n\t"                                                         \
-      "tcgen05.mma.cta_group::1." KIND " [dt], [at], db, %2, p;\n\t}" ::"r"(tmem),          \
+      "@e tcgen05.mma.cta_group::1." KIND " [dt], [at], db, %2, p;\n\t}" ::"r"(tmem),       \
       "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(kColD), "n"(kColA), "n"(kOffB),           \
       "n"(kSdescHi)                                                                         \
       : "memory")
@@ -271,10 +280,13 @@ __device__ __forceinline__ void mma_ts(uint32_t tmem, uint32_t b_lo, uint32_t id
 #undef ATTN_MMA_SS
 #undef ATTN_MMA_TS
 
-// Arrive on `bar` once every tcgen05 op issued so far by this thread completed.
+// Arrive on `bar` once every tcgen05 op issued so far by the issuing thread
+// completed.  Executed by the whole converged warp, like the MMA wrappers;
+// elect.sync over the full warp picks the thread that issued them.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
           smem_u32(bar))
       : "memory");
 }
