@@ -69,6 +69,12 @@ struct Cfg {
   static constexpr int kChunks = D * kElemBytes / 128;     // 128-byte swizzle chunks per tile row
   static constexpr int kStages = (D == 128) ? 4 : 8;       // K/V ring depth
   static constexpr int kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
+  // Q K^T in two N = 64 halves, keys [64, 128) issued while the softmax
+  // still works on the previous S (see the MMA warp).  Each half re-reads
+  // all of Q from shared memory, so the halves cost 3/4 of a full MMA's time
+  // each; that pays where the tensor pipe has slack (D = 64, e4m3) and not
+  // at D = 128 bf16, where it is already busy ~3/4 of the time.
+  static constexpr bool kSplitS = (D == 64) || kFp8;
   static constexpr int kTmemCols = 512;
   // P = 2^(s - m + kPBias) and the running max moves when it rises by more
   // than kRescale (log2 units).  bf16 P has fp32's range: any bias works, a
@@ -90,6 +96,7 @@ struct Misc {
   uint64_t q_full;        // the unit's Q tiles arrived (one phase per unit)
   uint64_t q_empty;       // the unit's last Q K^T retired: Q buffers reusable
   uint64_t s_full[2];     // S_t = Q_t K^T in TMEM (MMA commit)
+  uint64_t s_read[2];     // S_t loaded by the tile's softmax warps (one arrival per warp)
   uint64_t p_full[2];     // P_t in TMEM (one arrival per softmax warp of the tile)
   uint64_t o_done[2];     // every MMA of the unit's O_t retired (one phase per unit)
   uint64_t mma_done;
@@ -130,39 +137,48 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 // S = Q K^T over the head dimension into TMEM columns kColD, one MMA per 32
 // bytes of a row (16 bf16 or 32 e4m3 columns); inside a 128-byte swizzle
 // chunk a k-step advances the start address by 32 bytes, the next chunk
-// starts 128 rows * 128 bytes further.
-template <bool kFp8, uint32_t kColD, int KK, int NK>
-__device__ __forceinline__ void issue_s_rec(uint32_t tmem, uint32_t a0, uint32_t b0,
-                                            uint32_t idesc) {
+// starts 128 rows * 128 bytes further.  kOffB moves the K operand by whole
+// rows: kKeyHalf selects keys [64, 128) of the tile (64 rows * 128 bytes,
+// eight 1024-byte swizzle atoms).
+constexpr uint32_t kKeyHalf = (64 * 128) >> 4;
+template <bool kFp8, uint32_t kColD, uint32_t kOffA, uint32_t kOffB, uint32_t kIdesc, int KK,
+          int NK>
+__device__ __forceinline__ void issue_s_rec(uint32_t tmem, uint32_t a0, uint32_t b0) {
   if constexpr (KK < NK) {
     constexpr uint32_t off = ((KK >> 2) * (kBM * 128) + (KK & 3) * 32) >> 4;
-    mma_ss<kFp8, kColD, off, off>(tmem, a0, b0, idesc, KK > 0 ? 1u : 0u);
-    issue_s_rec<kFp8, kColD, KK + 1, NK>(tmem, a0, b0, idesc);
+    mma_ss<kFp8, kColD, off + kOffA, off + kOffB, kIdesc>(tmem, a0, b0, KK > 0 ? 1u : 0u);
+    issue_s_rec<kFp8, kColD, kOffA, kOffB, kIdesc, KK + 1, NK>(tmem, a0, b0);
   }
 }
-template <int D, bool kFp8, uint32_t kColD>
-__device__ __forceinline__ void issue_s_steps(uint32_t tmem, uint32_t a0, uint32_t b0,
-                                              uint32_t idesc) {
-  issue_s_rec<kFp8, kColD, 0, D * (kFp8 ? 1 : 2) / 32>(tmem, a0, b0, idesc);
+// N = 128 (all keys of the tile) or, with kHalf = 1 or 2, N = 64 over keys
+// [0, 64) or [64, 128) into the same columns of S as the full product.  The
+// A (Q) descriptor is a0 + kOffA (a constant, modulo 2^32, from the K ring's
+// descriptor, so that no second descriptor register stays live).
+template <int D, bool kFp8, uint32_t kColS, uint32_t kOffA, int kHalf = 0>
+__device__ __forceinline__ void issue_s_steps(uint32_t tmem, uint32_t a0, uint32_t b0) {
+  constexpr uint32_t kN = kHalf ? kBN / 2 : kBN;
+  constexpr uint32_t kIdesc = kFp8 ? idesc_e4m3_f32(128, kN) : idesc_bf16_f32(128, kN, false);
+  constexpr uint32_t kColD = kColS + (kHalf == 2 ? kBN / 2 : 0);
+  constexpr uint32_t kOffB = kHalf == 2 ? kKeyHalf : 0;
+  issue_s_rec<kFp8, kColD, kOffA, kOffB, kIdesc, 0, D * (kFp8 ? 1 : 2) / 32>(tmem, a0, b0);
 }
 // O (TMEM columns kColD) += P (TMEM columns kColP) V over the 128 keys of a
 // tile, one MMA per 8 TMEM columns of P (16 bf16 or 32 e4m3 keys).  bf16: V
 // is MN-major, a step advances 16 rows * 128 bytes.  e4m3: V^T (D rows of
 // 128 keys) is K-major, a step advances 32 bytes inside the 128-byte row.
-template <bool kFp8, uint32_t kColD, uint32_t kColP, int KK>
-__device__ __forceinline__ void issue_pv_rec(uint32_t tmem, uint32_t b0, uint32_t idesc,
-                                             uint32_t acc) {
+template <bool kFp8, uint32_t kColD, uint32_t kColP, uint32_t kOffB, uint32_t kIdesc, int KK>
+__device__ __forceinline__ void issue_pv_rec(uint32_t tmem, uint32_t b0, uint32_t acc) {
   constexpr int kSteps = kFp8 ? kBN / 32 : kBN / 16;
   if constexpr (KK < kSteps) {
     constexpr uint32_t off = kFp8 ? ((KK * 32) >> 4) : ((KK * 16 * 128) >> 4);
-    mma_ts<kFp8, kColD, kColP + KK * 8, off>(tmem, b0, idesc, KK > 0 ? 1u : acc);
-    issue_pv_rec<kFp8, kColD, kColP, KK + 1>(tmem, b0, idesc, acc);
+    mma_ts<kFp8, kColD, kColP + KK * 8, off + kOffB, kIdesc>(tmem, b0, KK > 0 ? 1u : acc);
+    issue_pv_rec<kFp8, kColD, kColP, kOffB, kIdesc, KK + 1>(tmem, b0, acc);
   }
 }
-template <bool kFp8, uint32_t kColD, uint32_t kColP>
-__device__ __forceinline__ void issue_pv_steps(uint32_t tmem, uint32_t b0, uint32_t idesc,
-                                               uint32_t acc) {
-  issue_pv_rec<kFp8, kColD, kColP, 0>(tmem, b0, idesc, acc);
+template <int D, bool kFp8, uint32_t kColD, uint32_t kColP, uint32_t kOffB>
+__device__ __forceinline__ void issue_pv_steps(uint32_t tmem, uint32_t b0, uint32_t acc) {
+  constexpr uint32_t kIdesc = kFp8 ? idesc_e4m3_f32(128, D) : idesc_bf16_f32(128, D, true);
+  issue_pv_rec<kFp8, kColD, kColP, kOffB, kIdesc, 0>(tmem, b0, acc);
 }
 
 // Work unit u: (batch*head, pair of 128-row query tiles).  Non-causal:
@@ -230,6 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&ms.q_empty, 1);
     for (int t = 0; t < 2; ++t) {
       mbar_init(&ms.s_full[t], 1);
+      mbar_init(&ms.s_read[t], 8);
       mbar_init(&ms.p_full[t], 8);
       mbar_init(&ms.o_done[t], 1);
     }
@@ -332,6 +349,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mx = max3f(a0, a1, fmaxf(a2, a3));
           mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));  // the row's other half
+        }
+        if constexpr (C::kSplitS) {
+          // S_t has been read (and used): the MMA warp may now write the next
+          // key tile's keys [64, 128) over columns 64..127 of S_t, which P
+          // does not use
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ms.s_read[t]);
         }
         // running max in log2 units (scale >= 0, so max commutes with scaling)
         const float m_tile = (mx == -CUDART_INF_F) ? -CUDART_INF_F : mx * p.scale_log2;
@@ -565,9 +590,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // =====================================================================
     reg_dealloc<kRegOther>();
     {
-      constexpr uint32_t idesc_s =
-          kFp8 ? idesc_e4m3_f32(128, kBN) : idesc_bf16_f32(128, kBN, false);
-      constexpr uint32_t idesc_pv = kFp8 ? idesc_e4m3_f32(128, D) : idesc_bf16_f32(128, D, true);
       constexpr uint32_t kTileDesc = C::kTileBytes >> 4;  // one tile in descriptor units
       // Descriptors are built once; every k-step only adds a constant to the
       // start-address field, so issuing an MMA costs a couple of instructions.
@@ -579,21 +601,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kVFromK = kFp8 ? 0u : static_cast<uint32_t>(((kBM * 128) >> 4) - 1) << 16;
       constexpr uint32_t kS = C::kStages;  // power of two
       static_assert((kS & (kS - 1)) == 0, "ring depth must be a power of two");
+      // Q_t's descriptor relative to the K ring's (a constant modulo 2^32)
+      constexpr uint32_t kQ0 = 0u - kQFromK, kQ1 = kQ0 + kTileDesc;
       // S_t = Q_t K^T from the K tile in ring slot `slot`
       auto issue_s = [&](int t, uint32_t slot) {
-        const uint32_t a0 = desc_k - kQFromK + static_cast<uint32_t>(t) * kTileDesc;
+        const uint32_t b0 = desc_k + slot * kTileDesc;
         if (t)
-          issue_s_steps<D, kFp8, C::kColS1>(tmem, a0, desc_k + slot * kTileDesc, idesc_s);
+          issue_s_steps<D, kFp8, C::kColS1, kQ1>(tmem, desc_k, b0);
         else
-          issue_s_steps<D, kFp8, C::kColS0>(tmem, a0, desc_k + slot * kTileDesc, idesc_s);
+          issue_s_steps<D, kFp8, C::kColS0, kQ0>(tmem, desc_k, b0);
+      };
+      // keys [64h, 64h + 64) of S_t = Q_t K^T into columns [64h, 64h + 64) of
+      // S_t.  Half 1 goes in as soon as the softmax warps have read S_t of the
+      // previous key tile (P_t takes columns below 64 only), half 0 after the
+      // P_t V that reads P_t from those columns: the tile's wait for its next
+      // S holds only the P V and half the Q K^T.
+      auto issue_s_half = [&](int t, uint32_t slot, int h) {
+        const uint32_t b0 = desc_k + slot * kTileDesc;
+        if (t) {
+          if (h)
+            issue_s_steps<D, kFp8, C::kColS1, kQ1, 2>(tmem, desc_k, b0);
+          else
+            issue_s_steps<D, kFp8, C::kColS1, kQ1, 1>(tmem, desc_k, b0);
+        } else {
+          if (h)
+            issue_s_steps<D, kFp8, C::kColS0, kQ0, 2>(tmem, desc_k, b0);
+          else
+            issue_s_steps<D, kFp8, C::kColS0, kQ0, 1>(tmem, desc_k, b0);
+        }
       };
       // O_t (+)= P_t V from the V tile in ring slot `slot`; P_t is in TMEM over S_t
       auto issue_pv = [&](int t, uint32_t slot, uint32_t acc) {
-        const uint32_t b0 = desc_k + kVFromK + slot * kTileDesc;
+        const uint32_t b0 = desc_k + slot * kTileDesc;
         if (t)
-          issue_pv_steps<kFp8, C::kColO1, C::kColS1>(tmem, b0, idesc_pv, acc);
+          issue_pv_steps<D, kFp8, C::kColO1, C::kColS1, kVFromK>(tmem, b0, acc);
         else
-          issue_pv_steps<kFp8, C::kColO0, C::kColS0>(tmem, b0, idesc_pv, acc);
+          issue_pv_steps<D, kFp8, C::kColO0, C::kColS0, kVFromK>(tmem, b0, acc);
       };
       int k = 0;  // units done
       // wait for P_t of global step gs (O_t is already rescaled when it arrives)
@@ -602,6 +645,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 p.wait_limit_ns)))
           return false;
         if (lane == 0 && k == 0) ATTN_TRACE_EV(5, t, jv);
+        tc_fence_after();
+        return true;
+      };
+      // wait until the softmax warps of tile t have read S_t of global step gs
+      auto wait_s_read = [&](int t, uint32_t gs) -> bool {
+        if (!warp_all(mbar_wait(&ms.s_read[t], gs & 1u, abort_flag, p.err, kErrWaitMma,
+                                p.wait_limit_ns)))
+          return false;
         tc_fence_after();
         return true;
       };
@@ -622,12 +673,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           tc_fence_after();
           for (int t = 0; t < 2 && ok; ++t) {
-            if (gs > step) {
+            if (gs > step && C::kSplitS) {
+              ok = wait_s_read(t, gs - 1);
+              if (!ok) break;
+              issue_s_half(t, sk, 1);
               ok = wait_p(t, gs - 1, static_cast<int>(gs - step) - 1);
               if (!ok) break;
               issue_pv(t, sv, gs > step + 1 ? 1u : 0u);
+              issue_s_half(t, sk, 0);
+            } else {
+              if (gs > step) {
+                ok = wait_p(t, gs - 1, static_cast<int>(gs - step) - 1);
+                if (!ok) break;
+                issue_pv(t, sv, gs > step + 1 ? 1u : 0u);
+              }
+              issue_s(t, sk);
             }
-            issue_s(t, sk);
             mma_commit(&ms.s_full[t]);
             if (lane == 0 && k == 0) ATTN_TRACE_EV(6, t, gs - step);
           }
@@ -645,7 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ok) {
             tc_fence_after();
             for (int t = 0; t < 2 && ok; ++t) {
-              ok = wait_p(t, gs, static_cast<int>(gs - step));
+              ok = (!C::kSplitS || wait_s_read(t, gs)) && wait_p(t, gs, static_cast<int>(gs - step));
               if (ok) {
                 issue_pv(t, sv, gs > step ? 1u : 0u);
                 mma_commit(&ms.o_done[t]);

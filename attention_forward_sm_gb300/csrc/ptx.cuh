@@ -217,8 +217,8 @@ __device__ __forceinline__ uint32_t sdesc_sw128_lo(uint32_t saddr, uint32_t lbo)
 
 // D[tmem] (+)= A[smem desc] * B[smem desc] (mma_ss) or A[tmem] * B[smem
 // desc] (mma_ts), kind::f16 (bf16 operands) or kind::f8f6f4 (e4m3).  Every
-// per-instruction offset is a compile-time constant added inside the
-// instruction group -- TMEM columns of D (and of A for mma_ts) to the TMEM
+// per-instruction offset and the instruction descriptor are compile-time
+// constants, the offsets added inside the instruction group -- TMEM columns of D (and of A for mma_ts) to the TMEM
 // base, 16-byte descriptor units to the descriptors' start addresses -- so
 // an unrolled sequence of MMAs keeps only the TMEM base and one descriptor
 // word live.  The whole (converged) warp executes these wrappers with
@@ -242,7 +242,7 @@ __device__ __forceinline__ uint32_t sdesc_sw128_lo(uint32_t saddr, uint32_t lbo)
       "or.b64 db, db, %8;\n\t"                                                            \
       "setp.ne.b32 p, %4, 0;\n\t"                                                         \
       "@e tcgen05.mma.cta_group::1." KIND " [dt], da, db, %3, p;\n\t}" ::"r"(tmem),         \
-      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(kColD), "n"(kOffA), "n"(kOffB), \
+      "r"(a_lo), "r"(b_lo), "n"(kIdesc), "r"(accumulate), "n"(kColD), "n"(kOffA), "n"(kOffB), \
       "n"(kSdescHi)                                                                         \
       : "memory")
 #define ATTN_MMA_TS(KIND)                                                                    \
@@ -256,22 +256,23 @@ __device__ __forceinline__ uint32_t sdesc_sw128_lo(uint32_t saddr, uint32_t lbo)
       "or.b64 db, db, %7;\n\t"                                                            \
       "setp.ne.b32 p, %3, 0;\n\t"                                                         \
       "@e tcgen05.mma.cta_group::1." KIND " [dt], [at], db, %2, p;\n\t}" ::"r"(tmem),       \
-      "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(kColD), "n"(kColA), "n"(kOffB),           \
+      "r"(b_lo), "n"(kIdesc), "r"(accumulate), "n"(kColD), "n"(kColA), "n"(kOffB),          \
       "n"(kSdescHi)                                                                         \
       : "memory")
-// D at TMEM column kColD, A and B descriptors (lower words) + kOffA, kOffB
-template <bool kF8, uint32_t kColD, uint32_t kOffA, uint32_t kOffB>
+// D at TMEM column kColD, A and B descriptors (lower words) + kOffA, kOffB,
+// instruction descriptor kIdesc
+template <bool kF8, uint32_t kColD, uint32_t kOffA, uint32_t kOffB, uint32_t kIdesc>
 __device__ __forceinline__ void mma_ss(uint32_t tmem, uint32_t a_lo, uint32_t b_lo,
-                                       uint32_t idesc, uint32_t accumulate) {
+                                       uint32_t accumulate) {
   if constexpr (kF8)
     ATTN_MMA_SS("kind::f8f6f4");
   else
     ATTN_MMA_SS("kind::f16");
 }
-// D at TMEM column kColD, A at TMEM column kColA, B descriptor (lower word) + kOffB
-template <bool kF8, uint32_t kColD, uint32_t kColA, uint32_t kOffB>
-__device__ __forceinline__ void mma_ts(uint32_t tmem, uint32_t b_lo, uint32_t idesc,
-                                       uint32_t accumulate) {
+// D at TMEM column kColD, A at TMEM column kColA, B descriptor (lower word) + kOffB,
+// instruction descriptor kIdesc
+template <bool kF8, uint32_t kColD, uint32_t kColA, uint32_t kOffB, uint32_t kIdesc>
+__device__ __forceinline__ void mma_ts(uint32_t tmem, uint32_t b_lo, uint32_t accumulate) {
   if constexpr (kF8)
     ATTN_MMA_TS("kind::f8f6f4");
   else
