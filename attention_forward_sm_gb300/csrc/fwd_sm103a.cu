@@ -20,9 +20,12 @@
 //   * one CTA = 2 query tiles of 128 rows of one (batch, head); the two tiles
 //     are independent MMA chains (the autoWS note's "data partitioning"), so
 //     the tensor core works on one tile while the softmax of the other runs;
-//   * tcgen05.mma (kind::f16, M=128) issued by a single thread; S = Q K^T and
-//     O accumulate in tensor memory (TMEM), not registers: S0, S1, O0, O1
-//     occupy 128 + 128 + D + D of the 512 TMEM columns;
+//   * tcgen05.mma (kind::f16, M=128) issued from one warp, one elected
+//     thread per instruction; S = Q K^T and O accumulate in tensor memory
+//     (TMEM), not registers: S0, S1, O0, O1 occupy 128 + 128 + D + D of the
+//     512 TMEM columns.  At D = 64 and for e4m3 the next key tile's
+//     Q K^T is issued in two halves, the upper one while the softmax still
+//     works on the current S;
 //   * P (bf16) is written back over S in TMEM and fed to the P*V MMA as the
 //     A operand straight from TMEM;
 //   * a TMA load warp streams K and V tiles (128 keys x D, 128-byte swizzle)

@@ -98,10 +98,17 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+KERNEL_HEADERS = ("ptx.cuh", "internal.h")  # included by every kernel file
+
+
 def kernel_source_hash(name: str) -> str:
-    path = os.path.join(ROOT, "attention_forward_sm_gb300", "csrc", name)
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """sha256 (first 16 hex digits) of a kernel source file and the headers
+    it includes: a profile taken before any of them changed is stale."""
+    h = hashlib.sha256()
+    for f in (name, *KERNEL_HEADERS):
+        with open(os.path.join(ROOT, "attention_forward_sm_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
 
 
 def profiled_traffic(kernel_file: str, key: str):
