@@ -682,7 +682,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               issue_s_half(t, sk, 1);
               ok = wait_p(t, gs - 1, static_cast<int>(gs - step) - 1);
               if (!ok) break;
-              issue_pv(t, sv, gs > step + 1 ? 1u : 0u);
+              // the accumulate flag as a constant in each branch keeps this
+              // path within the MMA warp's 32 registers (no spill at D = 64)
+              if (gs > step + 1)
+                issue_pv(t, sv, 1u);
+              else
+                issue_pv(t, sv, 0u);
               issue_s_half(t, sk, 0);
             } else {
               if (gs > step) {
