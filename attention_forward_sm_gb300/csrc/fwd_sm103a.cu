@@ -498,10 +498,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // =====================================================================
     // TMA loader: per unit the Q tiles (once the previous unit's last Q K^T
     // has read them), then K_j, V_j through the ring.  Ring item numbers run
-    // on across units: a unit's step j loads items 2(step + j), +1.
+    // on across units: a unit's step j loads items 2(step + j), +1.  The
+    // whole warp runs the loop (waits are warp-wide votes, so control flow
+    // stays uniform); one elected thread issues each copy, arrival and
+    // next-unit request.
     // =====================================================================
     reg_dealloc<kRegOther>();
-    if (lane == 0) {
+    {
       uint32_t item = 0;    // ring items of earlier units
       uint32_t g = 1;       // next ring item (the first unit's K_0 was issued during setup)
       uint32_t q_phase = 0;  // q_full phase of the last Q load issued
@@ -515,64 +518,65 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (; g < item_end; ++g) {
           const uint32_t it = g - item;  // item within the unit: K_{it/2} or V_{it/2}
           const uint32_t s = g % C::kStages;
-          if (!mbar_wait(&ms.kv_empty[s], ((g / C::kStages) & 1u) ^ 1u, abort_flag, p.err,
-                         kErrWaitLoad, p.wait_limit_ns)) {
+          if (!warp_all(mbar_wait(&ms.kv_empty[s], ((g / C::kStages) & 1u) ^ 1u, abort_flag,
+                                  p.err, kErrWaitLoad, p.wait_limit_ns))) {
             ok = false;
             break;
           }
-          if (k == 0) ATTN_TRACE_EV(7, it & 1, it >> 1);
-          mbar_arrive_expect_tx(&ms.kv_full[s], C::kTileBytes);
+          if (lane == 0 && k == 0) ATTN_TRACE_EV(7, it & 1, it >> 1);
+          mbar_arrive_expect_tx_elect(&ms.kv_full[s], C::kTileBytes);
           uint8_t* dst = smem + C::kOffKV + s * C::kTileBytes;
           const int jt = static_cast<int>(it >> 1);
           if (kFp8 && (it & 1)) {
             // V^T [D rows, keys]: rows 0..D-1, keys of tile jt
-            tma_load_3d(dst, &p.tmap_v, &ms.kv_full[s], jt * kBN, 0, bhkv,
-                        l2_policy_evict_last());
+            tma_load_3d_elect(dst, &p.tmap_v, &ms.kv_full[s], jt * kBN, 0, bhkv,
+                              l2_policy_evict_last());
           } else {
             const CUtensorMap* map = (it & 1) ? &p.tmap_v : &p.tmap_k;
             for (int ch = 0; ch < C::kChunks; ++ch)
-              tma_load_3d(dst + ch * (kBM * 128), map, &ms.kv_full[s], ch * C::kAtomElems,
-                          jt * kBN, bhkv, l2_policy_evict_last());
+              tma_load_3d_elect(dst + ch * (kBM * 128), map, &ms.kv_full[s], ch * C::kAtomElems,
+                                jt * kBN, bhkv, l2_policy_evict_last());
           }
           if (it == 0 && k > 0) {
             // the Q tiles of this unit, once the previous unit's last Q K^T
             // retired (its K_0 is already on the way)
-            if (!mbar_wait(&ms.q_empty, (k - 1) & 1, abort_flag, p.err, kErrWaitLoad,
-                           p.wait_limit_ns)) {
+            if (!warp_all(mbar_wait(&ms.q_empty, (k - 1) & 1, abort_flag, p.err, kErrWaitLoad,
+                                    p.wait_limit_ns))) {
               ok = false;
               ++g;
               break;
             }
             const Unit wq = decode_unit(p, u, ATTN_NQB);
             q_phase = k & 1;
-            mbar_arrive_expect_tx(&ms.q_full, 2 * C::kTileBytes);
+            mbar_arrive_expect_tx_elect(&ms.q_full, 2 * C::kTileBytes);
             for (int t = 0; t < 2; ++t)
               for (int ch = 0; ch < C::kChunks; ++ch)
-                tma_load_3d(smem + C::kOffQ + t * C::kTileBytes + ch * (kBM * 128), &p.tmap_q,
-                            &ms.q_full, ch * C::kAtomElems, wq.q_base + t * kBM, wq.bh,
-                            l2_policy_evict_first());
+                tma_load_3d_elect(smem + C::kOffQ + t * C::kTileBytes + ch * (kBM * 128),
+                                  &p.tmap_q, &ms.q_full, ch * C::kAtomElems,
+                                  wq.q_base + t * kBM, wq.bh, l2_policy_evict_first());
           }
         }
         item = item_end;
         if (!ok) break;
         // every load of unit k is issued: ask for the next unit (slot k % 2,
         // free once every role has read response k - 2)
-        if (k >= 2 && !mbar_wait(&ms.clc_empty[k & 1], ((k >> 1) + 1) & 1, abort_flag, p.err,
-                                 kErrWaitLoad, p.wait_limit_ns)) {
+        if (k >= 2 && !warp_all(mbar_wait(&ms.clc_empty[k & 1], ((k >> 1) + 1) & 1, abort_flag,
+                                          p.err, kErrWaitLoad, p.wait_limit_ns))) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&ms.clc_full[k & 1], 16);
-        clc_try_cancel(smem_u32(&ms.clc_resp[k & 1]), &ms.clc_full[k & 1]);
+        mbar_arrive_expect_tx_elect(&ms.clc_full[k & 1], 16);
+        clc_try_cancel_elect(smem_u32(&ms.clc_resp[k & 1]), &ms.clc_full[k & 1]);
         clc_k = k;
-        if (!mbar_wait(&ms.clc_full[k & 1], (k >> 1) & 1, abort_flag, p.err, kErrWaitLoad,
-                       p.wait_limit_ns)) {
+        if (!warp_all(mbar_wait(&ms.clc_full[k & 1], (k >> 1) & 1, abort_flag, p.err,
+                                kErrWaitLoad, p.wait_limit_ns))) {
           ok = false;
           break;
         }
         const int nu = clc_response_ctaid_x(smem_u32(&ms.clc_resp[k & 1]));
         fence_proxy_async_smem();
-        mbar_arrive(&ms.clc_empty[k & 1]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ms.clc_empty[k & 1]);
         if (nu < 0 || nu >= ATTN_UNITS) break;
         u = nu;
       }

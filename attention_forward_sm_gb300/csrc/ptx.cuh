@@ -97,6 +97,29 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// The same, executed by a whole converged warp with warp-uniform operands;
+// elect.sync picks the one thread that issues the copy (as for the MMAs
+// below: cheaper for the warp than a single-thread branch).
+__device__ __forceinline__ void tma_load_3d_elect(void* dst, const CUtensorMap* map,
+                                                  uint64_t* bar, int c0, int c1, int c2,
+                                                  uint64_t policy) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;\n\t}" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+// mbar_arrive_expect_tx by one elected thread of a converged warp.
+__device__ __forceinline__ void mbar_arrive_expect_tx_elect(uint64_t* bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(
+          smem_u32(bar)),
+      "r"(bytes)
+      : "memory");
+}
+
 // Generic-proxy shared-memory accesses ordered before later async-proxy ones.
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -110,6 +133,15 @@ __device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint64_t* bar) {
   asm volatile(
       "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 "
       "[%0], [%1];" ::"r"(resp),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+// clc_try_cancel by one elected thread of a converged warp.
+__device__ __forceinline__ void clc_try_cancel_elect(uint32_t resp, uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 "
+      "[%0], [%1];\n\t}" ::"r"(resp),
       "r"(smem_u32(bar))
       : "memory");
 }
