@@ -7,8 +7,11 @@ Builds a trace variant of the library (``-DATTN_TRACE``, in
 untouched), runs one launch, reads the stamps of the first 16 CTAs' first
 unit through ``attn_trace_copy`` and prints, per query tile, the softmax
 pass (S ready -> P published, with its load / max / exponential / store
-phases), the wait for the next S, the hand-offs to and from the MMA issuer
-and the step period, averaged over the middle key tiles.  The trace stores
+phases), the hand-off to the MMA warp, the time that warp takes to issue
+the tile's P V and next Q K^T, the rest of the wait for the next S, and the
+step period, averaged over the middle key tiles.  The pass is stamped by
+the tile's first warp; P is complete when the slowest warp of the tile has
+arrived, so the hand-off includes the spread between the tile's warps.  The trace stores
 cost a little time, so its periods run slightly long; benchmark numbers
 come from bench.py.
 """
@@ -79,14 +82,15 @@ def main():
     for t in range(2):
         e = lambda ev, d=0: np.array([[x[c, ev, t, j + d] for j in js] for c in range(CTAS)], float)
         s_ready, s_ld, s_max, s_exp, p_arr = e(0), e(1), e(2), e(3), e(4)
-        p_taken = e(5)           # the MMA issuer took P of key tile j
-        s_next = e(6, 1)         # it issued S of key tile j + 1 (after P V of tile j)
+        p_taken = e(5)           # the MMA warp took P of key tile j
+        s_next = e(6, 1)         # it had issued S of key tile j + 1 (after P V of tile j)
         s_ready_next = e(0, 1)   # softmax saw S of key tile j + 1
         print(f"  tile {t}: pass {np.mean(p_arr - s_ready):6.0f} (load {np.mean(s_ld - s_ready):4.0f},"
               f" max {np.mean(s_max - s_ld):4.0f}, exp {np.mean(s_exp - s_max):4.0f},"
               f" store+arrive {np.mean(p_arr - s_exp):4.0f});"
-              f" P -> issuer {np.mean(p_taken - p_arr):5.0f}; issuer P V + next Q K^T"
-              f" {np.mean(s_next - p_taken):5.0f}; S -> softmax {np.mean(s_ready_next - s_next):5.0f};"
+              f" P -> MMA warp {np.mean(p_taken - p_arr):5.0f}; P V + next Q K^T issued in"
+              f" {np.mean(s_next - p_taken):5.0f}; then S ready for the softmax after"
+              f" {np.mean(s_ready_next - s_next):5.0f};"
               f" step period {np.mean(np.diff(e(4), axis=1)):6.0f}")
 
 
