@@ -115,6 +115,20 @@ def test_full_size_sampled(name):
         assert torch.equal(o[:, :, 0, :], v0)
 
 
+def test_full_size_sampled_d64():
+    """The D = 64 benchmark shape (B8 H32 N8192, non-causal; the path that
+    issues half of the next Q K^T during the softmax pass), same launch as
+    the benchmark, >= 4096 sampled rows."""
+    w = W.custom(8, 32, 32, 8192, 8192, 64, False, seed_index=960)
+    q, k, v = W.make_inputs(w, "cuda")
+    o, lse = run_prefill(w, q, k, v)
+    assert attn.attn_get_device_error() == 0
+    rows = W.sample_rows(w, 4096)
+    assert rows.numel() >= 4096
+    o_ref, lse_ref = oracle_prefill(w, q, k, v, rows.numpy())
+    check(o.reshape(-1, w.D)[rows.cuda()], lse.reshape(-1)[rows.cuda()], o_ref, lse_ref, "d64")
+
+
 def test_causal_unit_groups_with_a_partial_last_group():
     """Causal units run in groups of whole KV heads sized to L2 (K+V of
     16.8 MB per KV head at Nk = 32768 gives two KV heads per group); with
