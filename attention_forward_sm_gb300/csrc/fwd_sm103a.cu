@@ -78,7 +78,14 @@ struct Cfg {
   // each; that pays where the tensor pipe has slack (D = 64, e4m3) and not
   // at D = 128 bf16, where it is already busy ~3/4 of the time.
   static constexpr bool kSplitS = (D == 64) || kFp8;
+  // D = 64 (bf16) has TMEM columns to spare: Q_t is copied there once per
+  // unit (kColQ0, kColQ1: D / 2 columns each) and every Q K^T reads A from
+  // TMEM, so an N = 64 half reads only its 2 KB of K from shared memory per
+  // k-step instead of 6 KB; Q's shared-memory buffers are free once copied.
+  static constexpr bool kQInTmem = (D == 64) && !kFp8;
+  static constexpr int kColQ0 = 2 * 128 + 2 * D, kColQ1 = kColQ0 + D / 2;
   static constexpr int kTmemCols = 512;
+  static_assert(!kQInTmem || kColQ1 + D / 2 <= kTmemCols, "TMEM columns");
   // P = 2^(s - m + kPBias) and the running max moves when it rises by more
   // than kRescale (log2 units).  bf16 P has fp32's range: any bias works, a
   // wide threshold saves O rescales.  E4M3 P saturates at 448 < 2^9, so
@@ -144,26 +151,33 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 // rows: kKeyHalf selects keys [64, 128) of the tile (64 rows * 128 bytes,
 // eight 1024-byte swizzle atoms).
 constexpr uint32_t kKeyHalf = (64 * 128) >> 4;
-template <bool kFp8, uint32_t kColD, uint32_t kOffA, uint32_t kOffB, uint32_t kIdesc, int KK,
-          int NK>
+// kColQ = 0: A (Q) from shared memory; otherwise A from TMEM columns
+// kColQ.. (Q copied there once per unit, 8 columns per k-step).
+template <bool kFp8, uint32_t kColD, uint32_t kOffA, uint32_t kColQ, uint32_t kOffB,
+          uint32_t kIdesc, int KK, int NK>
 __device__ __forceinline__ void issue_s_rec(uint32_t tmem, uint32_t a0, uint32_t b0) {
   if constexpr (KK < NK) {
     constexpr uint32_t off = ((KK >> 2) * (kBM * 128) + (KK & 3) * 32) >> 4;
-    mma_ss<kFp8, kColD, off + kOffA, off + kOffB, kIdesc>(tmem, a0, b0, KK > 0 ? 1u : 0u);
-    issue_s_rec<kFp8, kColD, kOffA, kOffB, kIdesc, KK + 1, NK>(tmem, a0, b0);
+    if constexpr (kColQ != 0)
+      mma_ts<kFp8, kColD, kColQ + KK * 8, off + kOffB, kIdesc>(tmem, b0, KK > 0 ? 1u : 0u);
+    else
+      mma_ss<kFp8, kColD, off + kOffA, off + kOffB, kIdesc>(tmem, a0, b0, KK > 0 ? 1u : 0u);
+    issue_s_rec<kFp8, kColD, kOffA, kColQ, kOffB, kIdesc, KK + 1, NK>(tmem, a0, b0);
   }
 }
 // N = 128 (all keys of the tile) or, with kHalf = 1 or 2, N = 64 over keys
 // [0, 64) or [64, 128) into the same columns of S as the full product.  The
 // A (Q) descriptor is a0 + kOffA (a constant, modulo 2^32, from the K ring's
-// descriptor, so that no second descriptor register stays live).
-template <int D, bool kFp8, uint32_t kColS, uint32_t kOffA, int kHalf = 0>
+// descriptor, so that no second descriptor register stays live), or, with
+// kColQ != 0, Q is read from TMEM columns kColQ..
+template <int D, bool kFp8, uint32_t kColS, uint32_t kOffA, int kHalf = 0, uint32_t kColQ = 0>
 __device__ __forceinline__ void issue_s_steps(uint32_t tmem, uint32_t a0, uint32_t b0) {
   constexpr uint32_t kN = kHalf ? kBN / 2 : kBN;
   constexpr uint32_t kIdesc = kFp8 ? idesc_e4m3_f32(128, kN) : idesc_bf16_f32(128, kN, false);
   constexpr uint32_t kColD = kColS + (kHalf == 2 ? kBN / 2 : 0);
   constexpr uint32_t kOffB = kHalf == 2 ? kKeyHalf : 0;
-  issue_s_rec<kFp8, kColD, kOffA, kOffB, kIdesc, 0, D * (kFp8 ? 1 : 2) / 32>(tmem, a0, b0);
+  issue_s_rec<kFp8, kColD, kOffA, kColQ, kOffB, kIdesc, 0, D * (kFp8 ? 1 : 2) / 32>(tmem, a0,
+                                                                                   b0);
 }
 // O (TMEM columns kColD) += P (TMEM columns kColP) V over the 128 keys of a
 // tile, one MMA per 8 TMEM columns of P (16 bf16 or 32 e4m3 keys).  bf16: V
@@ -611,12 +625,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Q_t's descriptor relative to the K ring's (a constant modulo 2^32)
       constexpr uint32_t kQ0 = 0u - kQFromK, kQ1 = kQ0 + kTileDesc;
       // S_t = Q_t K^T from the K tile in ring slot `slot`
+      constexpr uint32_t kTQ0 = C::kQInTmem ? C::kColQ0 : 0, kTQ1 = C::kQInTmem ? C::kColQ1 : 0;
       auto issue_s = [&](int t, uint32_t slot) {
         const uint32_t b0 = desc_k + slot * kTileDesc;
         if (t)
-          issue_s_steps<D, kFp8, C::kColS1, kQ1>(tmem, desc_k, b0);
+          issue_s_steps<D, kFp8, C::kColS1, kQ1, 0, kTQ1>(tmem, desc_k, b0);
         else
-          issue_s_steps<D, kFp8, C::kColS0, kQ0>(tmem, desc_k, b0);
+          issue_s_steps<D, kFp8, C::kColS0, kQ0, 0, kTQ0>(tmem, desc_k, b0);
       };
       // keys [64h, 64h + 64) of S_t = Q_t K^T into columns [64h, 64h + 64) of
       // S_t.  Half 1 goes in as soon as the softmax warps have read S_t of the
@@ -627,14 +642,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t b0 = desc_k + slot * kTileDesc;
         if (t) {
           if (h)
-            issue_s_steps<D, kFp8, C::kColS1, kQ1, 2>(tmem, desc_k, b0);
+            issue_s_steps<D, kFp8, C::kColS1, kQ1, 2, kTQ1>(tmem, desc_k, b0);
           else
-            issue_s_steps<D, kFp8, C::kColS1, kQ1, 1>(tmem, desc_k, b0);
+            issue_s_steps<D, kFp8, C::kColS1, kQ1, 1, kTQ1>(tmem, desc_k, b0);
         } else {
           if (h)
-            issue_s_steps<D, kFp8, C::kColS0, kQ0, 2>(tmem, desc_k, b0);
+            issue_s_steps<D, kFp8, C::kColS0, kQ0, 2, kTQ0>(tmem, desc_k, b0);
           else
-            issue_s_steps<D, kFp8, C::kColS0, kQ0, 1>(tmem, desc_k, b0);
+            issue_s_steps<D, kFp8, C::kColS0, kQ0, 1, kTQ0>(tmem, desc_k, b0);
         }
       };
       // O_t (+)= P_t V from the V tile in ring slot `slot`; P_t is in TMEM over S_t
@@ -669,6 +684,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (; ok; ++k) {
         const uint32_t step_end = step + static_cast<uint32_t>(decode_unit(p, u, ATTN_NQB).n_kv);
         ok = warp_all(mbar_wait(&ms.q_full, k & 1, abort_flag, p.err, kErrWaitMma, p.wait_limit_ns));
+        if constexpr (C::kQInTmem) {
+          // Q_0, Q_1 into TMEM (one 128 x 16 slice per copy; D = 64 is one
+          // 128-byte swizzle row, a slice advances 32 bytes).  The copies
+          // run in the tensor pipe ahead of this unit's Q K^T; they overwrite
+          // the previous unit's Q only once every MMA of that unit retired
+          // (its last P V, committed to o_done[1] after all its Q K^T), and
+          // Q's shared memory is free once they retire.
+          if (ok && k > 0)
+            ok = warp_all(mbar_wait(&ms.o_done[1], (k - 1) & 1, abort_flag, p.err, kErrWaitMma,
+                                    p.wait_limit_ns));
+          if (ok) {
+            tc_fence_after();
+            static_assert(D == 64, "one swizzle chunk per row");
+            const uint32_t q0 = desc_k + kQ0, q1 = desc_k + kQ1;
+            tmem_cp_128x256b<C::kColQ0 + 0, 0>(tmem, q0);
+            tmem_cp_128x256b<C::kColQ0 + 8, 2>(tmem, q0);
+            tmem_cp_128x256b<C::kColQ0 + 16, 4>(tmem, q0);
+            tmem_cp_128x256b<C::kColQ0 + 24, 6>(tmem, q0);
+            tmem_cp_128x256b<C::kColQ1 + 0, 0>(tmem, q1);
+            tmem_cp_128x256b<C::kColQ1 + 8, 2>(tmem, q1);
+            tmem_cp_128x256b<C::kColQ1 + 16, 4>(tmem, q1);
+            tmem_cp_128x256b<C::kColQ1 + 24, 6>(tmem, q1);
+            mma_commit(&ms.q_empty);
+          }
+        }
         // global step gs = step + j: K_j is ring item 2 gs, V_j item 2 gs + 1
         for (uint32_t gs = step; gs < step_end && ok; ++gs) {
           const uint32_t sk = (2u * gs) % kS, sv = (2u * gs - 1u) % kS;
@@ -709,7 +749,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (gs > step) mma_commit(&ms.kv_empty[sv]);
         }
         // the unit's last Q K^T is issued: Q's buffers are free once it retires
-        if (ok) mma_commit(&ms.q_empty);
+        if (ok && !C::kQInTmem) mma_commit(&ms.q_empty);
         if (ok) {
           const uint32_t gs = step_end - 1;
           const uint32_t sv = (2u * gs + 1u) % kS;

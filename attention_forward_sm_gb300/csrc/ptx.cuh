@@ -313,6 +313,26 @@ __device__ __forceinline__ void mma_ts(uint32_t tmem, uint32_t b_lo, uint32_t ac
 #undef ATTN_MMA_SS
 #undef ATTN_MMA_TS
 
+// Copy a 128-row x 256-bit slice of a shared-memory matrix (descriptor lower
+// word d_lo + kOff; upper word kSdescHi) into TMEM lanes 0..127, columns
+// kCol..kCol+7 of the base: row r lands in lane r, its 16 bf16 in column
+// order, two per column, the lower element in the low half -- the layout
+// an A operand in TMEM has.  Warp-wide, one elected thread issues; runs in
+// the tensor pipe in issue order with the MMAs of the same thread.
+template <uint32_t kCol, uint32_t kOff>
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t tmem, uint32_t d_lo) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b32 dt, dl;\n\t.reg .b64 d;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "add.u32 dt, %0, %2;\n\t"
+      "add.u32 dl, %1, %3;\n\t"
+      "cvt.u64.u32 d, dl;\n\t"
+      "or.b64 d, d, %4;\n\t"
+      "@e tcgen05.cp.cta_group::1.128x256b [dt], d;\n\t}" ::"r"(tmem),
+      "r"(d_lo), "n"(kCol), "n"(kOff), "n"(kSdescHi)
+      : "memory");
+}
+
 // Arrive on `bar` once every tcgen05 op issued so far by the issuing thread
 // completed.  Executed by the whole converged warp, like the MMA wrappers;
 // elect.sync over the full warp picks the thread that issued them.
