@@ -73,10 +73,11 @@ struct Cfg {
   static constexpr int kStages = (D == 128) ? 4 : 8;       // K/V ring depth
   static constexpr int kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
   // Q K^T in two N = 64 halves, keys [64, 128) issued while the softmax
-  // still works on the previous S (see the MMA warp).  Each half re-reads
-  // all of Q from shared memory, so the halves cost 3/4 of a full MMA's time
-  // each; that pays where the tensor pipe has slack (D = 64, e4m3) and not
-  // at D = 128 bf16, where it is already busy ~3/4 of the time.
+  // still works on the previous S (see the MMA warp).  With Q in shared
+  // memory each half re-reads all of Q, so the halves cost 3/4 of a full
+  // MMA's time each; that pays where the tensor pipe has slack (e4m3, and
+  // D = 64, whose Q moreover sits in TMEM) and not at D = 128 bf16, where
+  // the pipe is already busy ~3/4 of the time.
   static constexpr bool kSplitS = (D == 64) || kFp8;
   // D = 64 (bf16) has TMEM columns to spare: Q_t is copied there once per
   // unit (kColQ0, kColQ1: D / 2 columns each) and every Q K^T reads A from
@@ -104,7 +105,8 @@ struct Cfg {
 
 struct Misc {
   uint64_t q_full;        // the unit's Q tiles arrived (one phase per unit)
-  uint64_t q_empty;       // the unit's last Q K^T retired: Q buffers reusable
+  uint64_t q_empty;       // the unit's Q tiles were read (its last Q K^T, or with Q in
+                          // TMEM the copies, retired): Q buffers reusable
   uint64_t s_full[2];     // S_t = Q_t K^T in TMEM (MMA commit)
   uint64_t s_read[2];     // S_t loaded by the tile's softmax warps (one arrival per warp)
   uint64_t p_full[2];     // P_t in TMEM (one arrival per softmax warp of the tile)
