@@ -230,10 +230,47 @@ def attn_decode_workspace_bytes(B, Hq, D, nsplit) -> int:
 # ----------------------------------------------------------------------------- tensor helpers
 
 
+def _check_ranks(tensors: dict, ranks: dict):
+    import torch
+    for name, x in tensors.items():
+        if not isinstance(x, torch.Tensor):
+            raise TypeError(f"{name} must be a torch tensor")
+        if x.dim() != ranks[name]:
+            raise ValueError(f"{name} must have {ranks[name]} dimensions, got {x.dim()}")
+
+
+def _check_inputs(tensors: dict, shapes: dict):
+    """The helpers below pass raw pointers to the library, which cannot see
+    dtypes or strides: check here that every input is a contiguous bf16 CUDA
+    tensor, all on one device, with the expected ranks and matching sizes
+    (``shapes`` maps a size name to the values the tensors give it)."""
+    import torch
+    dev = None
+    for name, x in tensors.items():
+        if x.dtype != torch.bfloat16:
+            raise TypeError(f"{name} must be bfloat16, got {x.dtype}")
+        if not x.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not x.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if dev is None:
+            dev = x.device
+        elif x.device != dev:
+            raise ValueError(f"{name} is on {x.device}, expected {dev}")
+    for size, values in shapes.items():
+        if len(set(values)) != 1:
+            raise ValueError(f"inconsistent {size}: {values}")
+
+
+
 def forward(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
     """O, LSE = attention(q [B,Hq,Nq,D], k/v [B,Hkv,Nk,D]) with outputs
     allocated by torch on q's device."""
     import torch
+    _check_ranks({"q": q, "k": k, "v": v}, {"q": 4, "k": 4, "v": 4})  # [B, H, N, D]
+    _check_inputs({"q": q, "k": k, "v": v},
+                  {"B": (q.shape[0], k.shape[0], v.shape[0]), "D": (q.shape[3], k.shape[3], v.shape[3]),
+                   "Hkv": (k.shape[1], v.shape[1]), "Nk": (k.shape[2], v.shape[2])})
     B, Hq, Nq, D = q.shape
     Hkv, Nk = k.shape[1], k.shape[2]
     if scale is None:
@@ -252,6 +289,7 @@ class DecodeGraph:
     def __init__(self, q, kcache, vcache, nsplit: int):
         import torch
         self.handle = 0
+        _check_decode_inputs(q, kcache, vcache)
         B, Hq, D = q.shape
         Hkv, Nk = kcache.shape[1], kcache.shape[2]
         self.q, self.kcache, self.vcache = q, kcache, vcache
@@ -276,9 +314,19 @@ class DecodeGraph:
             pass
 
 
+def _check_decode_inputs(q, kcache, vcache):
+    # q [B, Hq, D], caches [B, Hkv, Nk, D]
+    _check_ranks({"q": q, "kcache": kcache, "vcache": vcache}, {"q": 3, "kcache": 4, "vcache": 4})
+    _check_inputs({"q": q, "kcache": kcache, "vcache": vcache},
+                  {"B": (q.shape[0], kcache.shape[0], vcache.shape[0]),
+                   "D": (q.shape[2], kcache.shape[3], vcache.shape[3]),
+                   "Hkv": (kcache.shape[1], vcache.shape[1]), "Nk": (kcache.shape[2], vcache.shape[2])})
+
+
 def decode(q, kcache, vcache, nsplit: int, stream=None):
     """O, LSE = split-KV decode(q [B,Hq,D], caches [B,Hkv,Nk,D])."""
     import torch
+    _check_decode_inputs(q, kcache, vcache)
     B, Hq, D = q.shape
     Hkv, Nk = kcache.shape[1], kcache.shape[2]
     o = torch.empty_like(q)

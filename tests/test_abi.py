@@ -155,3 +155,22 @@ def test_fwd_host_workspace_plan(lib):
     slot = 4 * 16 * per_head + 16 * 8192 * 4
     assert attn.attn_fwd_host_workspace_bytes(8, 32, 32, 8192, 8192, 128) == 2 * slot
     assert attn.attn_fwd_host_workspace_bytes(0, 32, 32, 8192, 8192, 128) == 0
+
+
+def test_tensor_helpers_reject_bad_inputs():
+    """forward / decode check dtype, device, contiguity and matching sizes
+    before any library call (the raw C-ABI names take pointers and cannot)."""
+    import torch
+    from attention_forward_sm_gb300 import binding as attn
+    q = torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        attn.forward(q, q, q)
+    with pytest.raises(TypeError, match="bfloat16"):
+        attn.forward(q.float(), q, q)
+    with pytest.raises(ValueError, match="dimensions"):
+        attn.forward(q[0], q, q)
+    q1 = torch.zeros(1, 2, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        attn.decode(q1, q, q, nsplit=2)
+    with pytest.raises(TypeError, match="torch tensor"):
+        attn.decode(q1, 0, q, nsplit=2)
