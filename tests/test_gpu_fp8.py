@@ -171,3 +171,26 @@ def test_fp8_correction_path(shape, construction):
         bound = 2.0 ** -8 * np.abs(o_ref) + 2.0 ** -12 * sc["v"] * v8.float().abs().max().item()
         bad = np.abs(og - o_ref) > bound
         assert not bad.any(), f"{label}: {int(bad.sum())} elements over the tight bound"
+
+
+def test_fp8_random_sweep():
+    """80 seeded random FP8 problems (Nk a multiple of 16, causal or not, GQA
+    groups 1-4, Nq 1-1800, scales up to 0.6), every row against the oracle
+    with the derived FP8 bound."""
+    rng = np.random.default_rng(20261204)
+    for ci in range(80):
+        G, Hkv = int(rng.choice([1, 2, 4])), int(rng.integers(1, 4))
+        B, Nq = int(rng.integers(1, 4)), int(rng.integers(1, 1800))
+        Nk = max(16, int(rng.integers(1, 2400)) // 16 * 16)
+        causal = bool(rng.integers(0, 2))
+        scale = float(rng.choice([1.0 / math.sqrt(128), 0.3, 0.05, 0.6]))
+        w = W.custom(B, Hkv * G, Hkv, Nq, Nk, 128, causal, seed_index=8000 + ci)
+        q8, k8, v8, vt8 = (t.cuda() for t in W.make_inputs_fp8(w, "cpu"))
+        o = torch.empty((w.B, w.Hq, w.Nq, w.D), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device="cuda")
+        attn.attn_fwd_fp8(q8, k8, vt8, o, lse, w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.D, w.causal, scale,
+                          SC["q"], SC["k"], SC["v"])
+        torch.cuda.synchronize()
+        assert attn.attn_get_device_error() == 0
+        check_fp8(w, o, lse, q8, k8, v8, label=f"case {ci}: {w.label()} scale {scale:.3f}",
+                  scale=scale)

@@ -435,3 +435,26 @@ def test_two_streams_at_once():
     for (w, q, k, v, o, lse) in data:
         o_ref, lse_ref = oracle_prefill(w, q, k, v)
         check(o, lse, o_ref.reshape(o.shape), lse_ref.reshape(lse.shape), w.label())
+
+
+def test_random_sweep_many_units():
+    """160 seeded random problems (D 64 or 128, causal or not, GQA groups 1-4,
+    B 1-3, Nq 1-1800, Nk 1-2400, scales up to 0.6 so that rescales happen),
+    every row against the oracle; with up to 3*12*8 units per launch, CTAs
+    also take over several units in turn."""
+    rng = np.random.default_rng(20261203)
+    for ci in range(160):
+        D = int(rng.choice([64, 128]))
+        G, Hkv = int(rng.choice([1, 2, 4])), int(rng.integers(1, 4))
+        B, Nq, Nk = int(rng.integers(1, 4)), int(rng.integers(1, 1800)), int(rng.integers(1, 2400))
+        causal = bool(rng.integers(0, 2))
+        scale = float(rng.choice([1.0 / math.sqrt(D), 0.3, 0.05, 0.6]))
+        w = W.custom(B, Hkv * G, Hkv, Nq, Nk, D, causal, seed_index=7000 + ci)
+        q, k, v = (t.cuda() for t in W.make_inputs(w, "cpu"))
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device="cuda")
+        attn.attn_fwd(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.D, w.causal, scale)
+        torch.cuda.synchronize()
+        assert attn.attn_get_device_error() == 0
+        o_ref, lse_ref = oracle_prefill(w, q, k, v, scale=scale)
+        check(o, lse, o_ref, lse_ref, f"case {ci}: {w.label()} scale {scale:.3f}")
