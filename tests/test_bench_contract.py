@@ -28,3 +28,26 @@ def test_reference_arm_json_line():
     e2e = d["e2e"]
     assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+import pytest  # noqa: E402
+
+
+@pytest.mark.gpu
+def test_main_arm_json_line():
+    """The main arm (one step, secondary workloads and host copies off)
+    prints the contract's keys: roofline, clocks, launch count, config."""
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--steps", "1",
+                          "--warmup", "3", "--no-e2e", "--no-cpu-baseline", "--no-other"],
+                         capture_output=True, text=True, timeout=900, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    d = json.loads([l for l in out.stdout.splitlines() if l.strip()][-1])
+    assert d["unit"] == "TFLOP/s" and d["value"] > 0 and d["dtype"] == "bf16"
+    assert d["n_gpus"] == 1 and d["steps"] == 1 and d["warmup"] == 3
+    assert d["config"]["workload"] and "l2" in d["config"]
+    r = d["roofline"]
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and r["peak"] > 0
+    assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-9
+    assert d["decode"]["roofline"]["bound"] == "hbm"
+    assert d["gpu_launches"] == 3 * d["steps"]
+    assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
